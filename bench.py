@@ -1,0 +1,517 @@
+#!/usr/bin/env python
+"""MoE-layer forward throughput on GB300: tokens/s of the whole hot path.
+
+One step = one pass of the layer over one batch held in HBM: gate GEMM + softmax +
+(grouped) top-K -> C_p prediction + token shuffle -> local-activation counts ->
+expert dispatch -> grouped SwiGLU FFN -> combine (-> next-layer prefetch predictor on
+the Qwen3-shaped FoE workload). Every stage is one C-ABI call of libsmoe.so; CUDA
+events between the calls give per-stage times inside the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Prints one JSON line (rank 0). Under torchrun every rank runs the same layer on its
+own seeded batch (replicas, weak scaling, no data-path collective); the timing is the
+maximum over ranks. ``--impl reference`` times the CPU oracle on this host instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "mixtral"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------- helpers
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--impl", default="native", choices=["native", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0,
+                   help="target CPU time of the oracle baseline sample")
+    return p.parse_args(argv)
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return world > 1
+
+
+def barrier(active: bool):
+    if active:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, active: bool, device="cpu") -> float:
+    """Maximum of a per-rank float over all ranks (identity on one rank)."""
+    if not active:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, seconds_max: float) -> float:
+    """Throughput of the whole job: units of all ranks over the slowest rank's time."""
+    return units_per_rank * world / seconds_max
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash(*names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "routing_token_shuffle_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def stage_bytes(cfg) -> dict:
+    """Algorithmic bytes per stage (each input read once, each output written once)."""
+    T, d, E, K, S, b = cfg.T, cfg.d, cfg.E, cfg.K, cfg.n_shared, cfg.elem_bytes
+    return {
+        "route": T * d * b + E * d * b + T * E * 4 + T * K * 8,
+        "predict_shuffle": T * 4 + T * E * 4 + 2 * T * d * b + 3 * T * 4,
+        "lar": T * K * 4 + T * 4,
+        "dispatch": 2 * T * K * d * b + T * K * 12,
+        "combine": T * K * d * b + S * T * d * b + T * K * 8 + T * d * b,
+    }
+
+
+def ffn_flops(cfg) -> float:
+    return 6.0 * cfg.d * cfg.F * (cfg.T * cfg.K + cfg.n_shared * cfg.T)
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.proc = None
+        self.path = None
+        self.gpu_id = gpu_id
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "200"]
+            if self.gpu_id:
+                cmd += ["-i", self.gpu_id]
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"),
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------- workload
+
+class Workload:
+    """Device-resident inputs of one workload and the per-stage C-ABI calls of a step."""
+
+    def __init__(self, name: str, device, rank: int = 0, prepare_with_oracle: bool = False):
+        import numpy as np
+        import torch
+
+        import routing_token_shuffle_gb300 as smoe
+        from routing_token_shuffle_gb300 import profiling, synth
+
+        self.smoe = smoe
+        cfg = synth.CONFIGS[name]
+        self.cfg = cfg
+        dev = torch.device(device)
+        self.dev = dev
+        self.emb = synth.Embedding(cfg, dev)
+        self.ids, x32 = synth.token_batch(cfg, self.emb, "ids", cfg.T, dev, salt=rank)
+        self.x = x32.to(cfg.torch_dtype).contiguous()
+        del x32
+        self.w_gate, self.w1, self.w3, self.w2 = synth.layer_weights_lowp(cfg, dev)
+        self.emap = synth.placement_identity(cfg)
+        self.desc = smoe.desc_from_config(cfg)
+        self.ws = None if prepare_with_oracle else smoe.workspace(self.desc, dev)
+        # offline C_p: route a seeded profiling batch with the library, count on the host
+        n_prof = cfg.profile_tokens
+        pids, px = synth.token_batch(cfg, self.emb, "profile", n_prof, dev)
+        px = px.to(cfg.torch_dtype)
+        if prepare_with_oracle:
+            import oracle as O
+            _, self.profile_idx, _ = O.route(px.float().cpu().numpy(),
+                                             self.w_gate.float().cpu().numpy(), cfg.K, cfg.H)
+        else:
+            pdesc = smoe.desc_from_config(cfg, T=n_prof)
+            pidx = torch.empty(n_prof, cfg.K, dtype=torch.int32, device=dev)
+            pw = torch.empty(n_prof, cfg.K, device=dev)
+            plog = torch.empty(n_prof, cfg.E, device=dev)
+            smoe.smoe_route(pdesc, px, self.w_gate, pidx, pw, logits_out=plog)
+            self.profile_idx = pidx.cpu().numpy()
+            del pw, plog
+        del px
+        self.conf = profiling.confidence_table(
+            pids, self.profile_idx, cfg.vocab, cfg.E, cfg.K,
+            emb_rows=lambda v: self.emb.rows(v).cpu().numpy(), rows_needed=self.ids)
+        self.conf_d = torch.as_tensor(self.conf, device=dev)
+        self.emap_d = torch.as_tensor(self.emap, device=dev)
+        self.ids_d = torch.as_tensor(self.ids, device=dev)
+        T, K, E, P = cfg.T, cfg.K, cfg.E, cfg.P
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.logits = torch.empty(T, E, device=dev)
+        self.idx = torch.empty(T, K, **i32)
+        self.w = torch.empty(T, K, device=dev)
+        self.pred = torch.empty(T, **i32)
+        self.perm = torch.empty(T, **i32)
+        self.part_off = torch.empty(P + 1, **i32)
+        self.lar = torch.zeros(4, dtype=torch.int64, device=dev)
+        self.expert_off = torch.empty(E + 1, **i32)
+        self.pair_row = torch.empty(T, K, **i32)
+        self.row_token = torch.empty(T * K, **i32)
+        self.x_shuf = torch.empty_like(self.x)
+        self.x_disp = torch.empty(T * K, cfg.d, dtype=self.x.dtype, device=dev)
+        self.y_sh = (torch.empty(cfg.n_shared, T, cfg.d, dtype=self.x.dtype, device=dev)
+                     if cfg.n_shared else None)
+        self.y = torch.empty_like(self.x)
+        self.weights = smoe.layer_weights(self.w_gate, self.w1, self.w3, self.w2, self.conf_d,
+                                          self.emap_d)
+        self.prefetch = None
+        if cfg.prefetch and not prepare_with_oracle:
+            r, wgn, gamma, beta = synth.predictor_inputs(cfg, dev)
+            # default vector d_l: mean layer output over a separate 1024-token batch
+            _, xp = synth.profile_batch_for_default_vector(cfg, self.emb, dev)
+            xp = xp.to(cfg.torch_dtype)
+            dd = smoe.desc_from_config(cfg, T=xp.shape[0])
+            wsd = smoe.workspace(dd, dev)
+            yp = torch.empty_like(xp)
+            ids_p = torch.zeros(xp.shape[0], dtype=torch.int32, device=dev)
+            smoe.smoe_layer_forward(dd, self.weights, smoe.layer_io(xp, ids_p, yp), wsd)
+            d_l = yp.float().mean(dim=0).contiguous()
+            del wsd, xp, yp
+            self.prefetch = dict(r=r, d_l=d_l, wgn=wgn.to(cfg.torch_dtype), gamma=gamma, beta=beta,
+                                 pi=torch.empty(T, K, **i32), ti=torch.empty(T, K, **i32),
+                                 hits=torch.zeros(1, dtype=torch.int64, device=dev))
+        torch.cuda.synchronize()
+
+    STAGES = ("route", "predict_shuffle", "lar", "dispatch", "expert_ffn", "combine", "prefetch")
+
+    def step(self, events=None):
+        """One forward of the layer; records an event after each stage when given."""
+        s, c = self.smoe, self
+        rec = (lambda i: events[i].record()) if events is not None else (lambda i: None)
+        s.smoe_route(c.desc, c.x, c.w_gate, c.idx, c.w, logits_out=c.logits, ws=c.ws)
+        rec(0)
+        s.smoe_predict_shuffle(c.desc, c.ids_d, c.conf_d, c.emap_d, c.pred, c.perm, c.part_off,
+                               c.ws, x=c.x, x_shuf=c.x_shuf)
+        rec(1)
+        s.smoe_lar(c.desc, c.idx, c.emap_d, c.lar, c.ws, src_part=c.pred)
+        rec(2)
+        s.smoe_dispatch(c.desc, c.idx, c.expert_off, c.pair_row, c.row_token, c.ws,
+                        shuf_perm=c.perm, x_src=c.x_shuf, x_disp=c.x_disp)
+        rec(3)
+        s.smoe_expert_ffn(c.desc, c.x_disp, c.expert_off, c.w1, c.w3, c.w2, c.x_disp, c.ws,
+                          x=c.x, y_shared=c.y_sh)
+        rec(4)
+        s.smoe_combine(c.desc, c.x_disp, c.pair_row, c.w, c.y, c.ws, y_shared=c.y_sh)
+        rec(5)
+        if c.prefetch is not None:
+            p = c.prefetch
+            s.smoe_prefetch_predict(c.desc, p["r"], p["d_l"], c.y, p["gamma"], p["beta"], p["wgn"],
+                                    p["pi"], p["ti"], p["hits"], c.ws)
+        rec(6)
+
+
+# ----------------------------------------------------------------- CPU oracle
+
+def cpu_oracle_rate(wl, target_s: float, max_tokens: int | None = None):
+    """Tokens/s of the CPU oracle on the first n tokens of the workload's batch, n sized
+    so one timed pass takes about target_s seconds. Returns (rate, n, seconds, cores)."""
+    import numpy as np
+
+    import oracle as O
+    cfg = wl.cfg
+    x = wl.x.float().cpu().numpy()
+    wg = wl.w_gate.float().cpu().numpy()
+    w1 = wl.w1.float().cpu().numpy()
+    w3 = wl.w3.float().cpu().numpy()
+    w2 = wl.w2.float().cpu().numpy()
+    ids, conf, emap = wl.ids, wl.conf, wl.emap
+    cap = cfg.T if max_tokens is None else min(cfg.T, max_tokens)
+
+    def run(n):
+        t0 = time.perf_counter()
+        O.layer_forward(x[:n], ids[:n], wg, w1, w3, w2, conf, emap, K=cfg.K, H=cfg.H, P=cfg.P,
+                        n_shared=cfg.n_shared)
+        return time.perf_counter() - t0
+
+    n = min(cap, 16)
+    t = run(n)
+    while t < target_s / 4 and n < cap:
+        n = min(cap, max(n * 2, int(n * target_s / max(t, 1e-3) * 0.8)))
+        t = run(n)
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return n / t, n, t, cores
+
+
+# ----------------------------------------------------------------- arms
+
+def run_native(args):
+    import torch
+
+    import routing_token_shuffle_gb300 as smoe
+    from routing_token_shuffle_gb300 import build as build_mod
+
+    rank, world, local_rank = dist_env()
+    world = max(world, 1)
+    if world != args.gpus and world > 1:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE {world}")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if rank == 0:
+        build_mod.build()
+    active = init_dist(world, "nccl")
+    barrier(active)
+    build_mod.build()
+    wl = Workload(args.workload, dev, rank=rank)
+    cfg = wl.cfg
+    peaks, peaks_kind = load_peaks()
+
+    for _ in range(max(args.warmup, 3)):
+        wl.step()
+    smoe.smoe_get_status(wl.ws)
+    torch.cuda.synchronize()
+
+    nst = len(Workload.STAGES)
+    start = torch.cuda.Event(enable_timing=True)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst)] for _ in range(args.steps)]
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(uuid)
+    barrier(active)
+    torch.cuda.synchronize()
+    sampler.start()
+    launches0 = smoe.kernel_launches()
+    wall0 = time.perf_counter()
+    start.record()
+    for i in range(args.steps):
+        wl.step(evs[i])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    launches = smoe.kernel_launches() - launches0
+    barrier(active)
+    clocks = sampler.stop()
+    total_ms = start.elapsed_time(evs[-1][-1])
+    stage_ms = {s: 0.0 for s in Workload.STAGES}
+    for i in range(args.steps):
+        prev = start if i == 0 else evs[i - 1][-1]
+        for j, sname in enumerate(Workload.STAGES):
+            stage_ms[sname] += prev.elapsed_time(evs[i][j])
+            prev = evs[i][j]
+    stage_ms = {k: v / args.steps for k, v in stage_ms.items()}
+    total_ms_max = max_over_ranks(total_ms, active, device=dev)
+    ms_per_step = total_ms_max / args.steps
+    value = whole_job_rate(cfg.T * args.steps, world, total_ms_max / 1e3)
+    smoe.smoe_get_status(wl.ws)
+
+    # end to end through the host-buffer entry point: H2D of x and ids, D2H of y
+    xh = wl.x.cpu().pin_memory()
+    ih = torch.as_tensor(wl.ids).pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    for _ in range(2):
+        smoe.smoe_layer_forward_host(wl.desc, wl.weights, xh, ih, yh, wl.ws)
+    torch.cuda.synchronize()
+    barrier(active)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        smoe.smoe_layer_forward_host(wl.desc, wl.weights, xh, ih, yh, wl.ws)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), active, device=dev)
+    e2e_value = whole_job_rate(cfg.T * args.steps, world, e2e_ms / 1e3)
+    h2d = xh.numel() * xh.element_size() + ih.numel() * ih.element_size()
+    d2h = yh.numel() * yh.element_size()
+
+    # roofline of the dominant kernel: the grouped expert FFN GEMMs
+    ffn_ms = stage_ms["expert_ffn"]
+    peak_tf = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    achieved_tf = ffn_flops(cfg) / (ffn_ms / 1e3) / 1e12
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "expert_ffn_traffic.json")
+    if os.path.exists(tfile):
+        with open(tfile) as f:
+            tj = json.load(f)
+        if tj.get("source_hash") == source_hash("ffn.cu") and tj.get("workload") == cfg.name:
+            traffic = tj.get("bytes_per_step")
+    roofline = {"bound": "tensor", "achieved": round(achieved_tf, 2), "peak": peak_tf,
+                "unit": "TFLOP/s", "frac": round(achieved_tf / peak_tf, 4), "traffic": traffic,
+                "kernel": "expert_ffn (grouped SwiGLU up + down GEMMs)",
+                "peak_kind": f"{peaks_kind} bf16 sustained"}
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    sb = stage_bytes(cfg)
+    stages = {}
+    for k, ms in stage_ms.items():
+        ent = {"ms": round(ms, 4)}
+        if k in sb and ms > 0:
+            gbs = sb[k] / (ms / 1e3) / 1e9
+            ent.update({"GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4)})
+        stages[k] = ent
+    stages["expert_ffn"]["TFLOP/s"] = round(achieved_tf, 2)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, n, secs, cores = cpu_oracle_rate(wl, args.cpu_seconds)
+        cpu = {"value": round(rate, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"first {n} of the {cfg.T} tokens of this workload's batch, the whole "
+                         f"layer in float64 numpy ({secs:.1f} s)"}
+    lar = wl.lar.cpu().numpy()
+    result = {
+        "metric": "MoE-layer tokens/s (gate+top-K, s-TS predict+shuffle, LAR, dispatch, grouped "
+                  "SwiGLU FFN, combine) on GB300",
+        "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype,
+        "data": "synthetic (seeded; random-init weights of the workload's shape)",
+        "config": {"workload": f"{cfg.name}: T={cfg.T}, d={cfg.d}, E={cfg.E}, K={cfg.K}, "
+                               f"H={cfg.H}, F={cfg.F}, shared={cfg.n_shared}, P={cfg.P}, "
+                               f"vocab={cfg.vocab}",
+                   "global_batch": cfg.T * world, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (expert weights "
+                         f"{3 * (cfg.E + cfg.n_shared) * cfg.F * cfg.d * cfg.elem_bytes / 1e9:.2f}"
+                         " GB streamed every step)"},
+        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches),
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+        "stages": stages,
+        "alpha": {"sTS": float(lar[0] / lar[1]), "base": float(lar[2] / lar[1]),
+                  "max": float(lar[3] / lar[1])},
+        "wall_s_timed": round(wall, 3),
+    }
+    if wl.prefetch is not None:
+        result["prefetch_hit_rate"] = float(wl.prefetch["hits"].item() / (cfg.T * cfg.K))
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if active:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The CPU oracle as it stands, on this host's cores, same workload and metric."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import torch
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    wl = Workload(args.workload, dev, prepare_with_oracle=True)
+    per_step = max(1.0, min(args.cpu_seconds, 150.0 / max(args.steps + args.warmup, 1)))
+    rate, n, secs, cores = cpu_oracle_rate(wl, per_step)
+    import oracle as O
+    cfg = wl.cfg
+    x = wl.x.float().cpu().numpy()[:n]
+    wg = wl.w_gate.float().cpu().numpy()
+    w1, w3, w2 = (t.float().cpu().numpy() for t in (wl.w1, wl.w3, wl.w2))
+    for _ in range(args.warmup):
+        O.layer_forward(x, wl.ids[:n], wg, w1, w3, w2, wl.conf, wl.emap, K=cfg.K, H=cfg.H,
+                        P=cfg.P, n_shared=cfg.n_shared)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        O.layer_forward(x, wl.ids[:n], wg, w1, w3, w2, wl.conf, wl.emap, K=cfg.K, H=cfg.H,
+                        P=cfg.P, n_shared=cfg.n_shared)
+    secs = time.perf_counter() - t0
+    value = n * args.steps / secs
+    sample = (f"first {n} of the {cfg.T} tokens of the batch per step, whole layer in float64 "
+              f"numpy")
+    print(json.dumps({
+        "impl": "reference",
+        "metric": "MoE-layer tokens/s (gate+top-K, s-TS predict+shuffle, LAR, dispatch, grouped "
+                  "SwiGLU FFN, combine) on GB300",
+        "value": round(value, 3), "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": f"{cfg.name}: T={cfg.T}, d={cfg.d}, E={cfg.E}, K={cfg.K}, "
+                               f"H={cfg.H}, F={cfg.F}, shared={cfg.n_shared}, P={cfg.P}",
+                   "global_batch": n},
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,11 @@
+"""GB300-native MoE-layer forward pass with speculative token shuffling.
+
+The compute lives in ``lib/libsmoe.so`` (hand-written CUDA for sm_103a behind the C
+ABI of ``include/smoe.h``); ``binding`` forwards tensors to it. Build it with
+``routing_token_shuffle_gb300.build.build()``.
+"""
+from .binding import (  # noqa: F401
+    SMOE_BF16, SMOE_F32, LayerIO, LayerWeights, SmoeDesc, SmoeError, desc_from_config, kernel_launches, layer_io,
+    layer_weights, lib, make_desc, smoe_combine, smoe_dispatch, smoe_expert_ffn, smoe_get_status,
+    smoe_lar, smoe_layer_forward, smoe_layer_forward_host, smoe_predict_shuffle,
+    smoe_prefetch_predict, smoe_route, workspace, workspace_size)

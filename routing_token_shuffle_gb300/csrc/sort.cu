@@ -1,0 +1,425 @@
+// Predicted-partition lookup, stable counting sorts (token shuffle and expert
+// dispatch), row gathers and local-activation counts.
+//
+// "Speculative MoE" §3.1 (s-TS: move each token ahead of time to the partition of
+// its predicted experts), §4.1 (C_p = Pr(E_k | token) looked up by token id), §1
+// (EP dispatch into the experts' devices), §2/§7 (local activation rate), and the
+// FoE article's grouped layout for the source partition of a token copy.
+//
+// A counting sort is three launches with no inter-CTA waiting: per-tile bucket
+// histograms, one CTA scanning the (bucket, tile) table, and a scatter that ranks
+// each tile's elements stably (warp match + per-warp counts in shared memory).
+#include <algorithm>
+
+#include "smoe_internal.cuh"
+
+namespace smoe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxBuckets = 512;
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// ------------------------------------------------------------------ predict
+// One tile of kSortTile tokens per CTA, one warp per token: the warp stages the
+// token's C_p row in shared memory, lane p sums its partition's experts in
+// ascending e (one fp32 add each), and a butterfly argmax with the order
+// (score descending, partition ascending) picks pred[t]. Also counts the tile's
+// histogram of predicted partitions.
+__global__ void __launch_bounds__(kThreads)
+predict_hist_kernel(const int32_t* __restrict__ ids, const float* __restrict__ conf,
+                    const int32_t* __restrict__ emap, int T, int E, int P, int vocab,
+                    int32_t* __restrict__ pred, int32_t* __restrict__ hist, int ntiles,
+                    DeviceStatus* st) {
+  __shared__ int s_list[kMaxBuckets];
+  __shared__ int s_start[33];
+  __shared__ int s_cnt[32];
+  __shared__ float s_row[kWarps][kMaxBuckets];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid < 32) s_cnt[tid] = 0;
+  if (warp == 0) {
+    int c = 0;
+    for (int e = 0; e < E; ++e) c += (lane < P && emap[e] == lane);
+    int incl = c;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    int pos = incl - c;
+    if (lane < P) s_start[lane] = pos;
+    if (lane == P - 1) s_start[P] = incl;
+    for (int e = 0; e < E; ++e)
+      if (lane < P && emap[e] == lane) s_list[pos++] = e;
+    if (blockIdx.x == 0 && lane == 0)
+      for (int e = 0; e < E; ++e)
+        if (emap[e] < 0 || emap[e] >= P) record_error(st, kStatusData, kBadExpertPart, e);
+  }
+  __syncthreads();
+
+  const int t0 = blockIdx.x * kSortTile;
+  const int t1 = min(t0 + kSortTile, T);
+  for (int t = t0 + warp; t < t1; t += kWarps) {
+    const int id = ids[t];
+    int best = 0;
+    if ((unsigned)id < (unsigned)vocab) {
+      const float* row = conf + (size_t)id * E;
+      for (int e = lane; e < E; e += 32) s_row[warp][e] = __ldg(row + e);
+      __syncwarp();
+      float sc = -INFINITY;
+      if (lane < P) {
+        float acc = 0.0f;
+        for (int i = s_start[lane]; i < s_start[lane + 1]; ++i) acc = acc + s_row[warp][s_list[i]];
+        sc = acc;
+      }
+      int bi = lane;
+#pragma unroll
+      for (int off = 16; off; off >>= 1) {
+        const float os = __shfl_xor_sync(0xffffffffu, sc, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (os > sc || (os == sc && oi < bi)) { sc = os; bi = oi; }
+      }
+      // only a NaN/inf row (outside the contract) can leave a lane >= P in front
+      best = (unsigned)bi < (unsigned)P ? bi : 0;
+      __syncwarp();
+    } else if (lane == 0) {
+      record_error(st, kStatusData, kBadTokenId, t);
+    }
+    if (lane == 0) {
+      pred[t] = best;
+      atomicAdd(&s_cnt[best], 1);
+    }
+  }
+  __syncthreads();
+  if (tid < P) hist[tid * ntiles + blockIdx.x] = s_cnt[tid];
+}
+
+// ------------------------------------------------------------------ dispatch hist
+// Pairs q = s K + k in shuffled-slot order; bucket = expert idx[perm[s], k].
+__global__ void __launch_bounds__(kThreads)
+dispatch_hist_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ perm, int T,
+                     int K, int E, int32_t* __restrict__ bucket, int32_t* __restrict__ hist,
+                     int ntiles, DeviceStatus* st) {
+  __shared__ int s_cnt[kMaxBuckets];
+  const int tid = threadIdx.x;
+  for (int b = tid; b < E; b += kThreads) s_cnt[b] = 0;
+  __syncthreads();
+  const long long n = (long long)T * K;
+  const long long q0 = (long long)blockIdx.x * kSortTile;
+  const long long q1 = min(q0 + kSortTile, n);
+  for (long long q = q0 + tid; q < q1; q += kThreads) {
+    const int s = (int)(q / K), k = (int)(q - (long long)s * K);
+    const int t = perm ? perm[s] : s;
+    int e = 0;
+    if ((unsigned)t >= (unsigned)T) {
+      record_error(st, kStatusData, kBadPerm, s);
+    } else {
+      e = idx[(size_t)t * K + k];
+      if ((unsigned)e >= (unsigned)E) {
+        record_error(st, kStatusData, kBadTopkIdx, (long long)t * K + k);
+        e = 0;
+      }
+    }
+    bucket[q] = e;
+    atomicAdd(&s_cnt[e], 1);
+  }
+  __syncthreads();
+  for (int b = tid; b < E; b += kThreads) hist[b * ntiles + blockIdx.x] = s_cnt[b];
+}
+
+// ------------------------------------------------------------------ scan
+// One CTA: exclusive scan of the bucket-major (bucket, tile) histogram, giving each
+// tile's first output position per bucket; bucket_off[b] = start of bucket b.
+__global__ void __launch_bounds__(1024)
+scan_kernel(const int32_t* __restrict__ hist, int32_t* __restrict__ offs, int L, int B,
+            int ntiles, int n, int32_t* __restrict__ bucket_off) {
+  __shared__ int s_warp[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (L + blockDim.x - 1) / blockDim.x;
+  const int lo = min(tid * per, L), hi = min(lo + per, L);
+  int sum = 0;
+  for (int i = lo; i < hi; ++i) sum += hist[i];
+  int x = sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int v = lane < (int)(blockDim.x >> 5) ? s_warp[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, v, off);
+      if (lane >= off) v += y;
+    }
+    s_warp[lane] = v;
+  }
+  __syncthreads();
+  int run = x - sum + (warp > 0 ? s_warp[warp - 1] : 0);
+  for (int i = lo; i < hi; ++i) {
+    const int v = hist[i];
+    offs[i] = run;
+    run += v;
+  }
+  __syncthreads();
+  for (int b = tid; b < B; b += blockDim.x) bucket_off[b] = offs[b * ntiles];
+  if (tid == 0) bucket_off[B] = n;
+}
+
+// ------------------------------------------------------------------ scatter
+// Stable rank of every element of a tile within its bucket: chunks of kThreads
+// elements in index order; inside a chunk, warps in order, inside a warp, lanes in
+// order (warp match gives the peers of equal bucket).
+enum ScatterMode { kShuffle = 0, kDispatch = 1 };
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads)
+scatter_kernel(const int32_t* __restrict__ bucket, int n, int B, int ntiles,
+               const int32_t* __restrict__ offs,
+               // kShuffle: perm_out[pos] = i
+               int32_t* __restrict__ perm_out,
+               // kDispatch
+               const int32_t* __restrict__ perm_in, int T, int K, int32_t* __restrict__ pair_row,
+               int32_t* __restrict__ row_token, int32_t* __restrict__ row_src) {
+  __shared__ int s_run[kMaxBuckets];
+  __shared__ int s_wc[kWarps][kMaxBuckets];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int b = tid; b < B; b += kThreads) {
+    s_run[b] = offs[b * ntiles + blockIdx.x];
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) s_wc[w][b] = 0;
+  }
+  __syncthreads();
+  const int base = blockIdx.x * kSortTile;
+  for (int c = 0; c < kSortTile && base + c < n; c += kThreads) {
+    const int i = base + c + tid;
+    const bool valid = i < n;
+    const int b = valid ? bucket[i] : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, b);
+    const int rank = __popc(peers & lanemask_lt());
+    if (valid && rank == 0) s_wc[warp][b] = __popc(peers);
+    __syncthreads();
+    if (valid) {
+      int pos = s_run[b] + rank;
+      for (int w = 0; w < warp; ++w) pos += s_wc[w][b];
+      if (MODE == kShuffle) {
+        perm_out[pos] = i;
+      } else {
+        const int s = i / K, k = i - s * K;
+        const int t = perm_in ? perm_in[s] : s;
+        const bool tok_ok = (unsigned)t < (unsigned)T;
+        if (tok_ok) pair_row[(size_t)t * K + k] = pos;
+        row_token[pos] = tok_ok ? t : -1;
+        row_src[pos] = s;
+      }
+    }
+    __syncthreads();
+    for (int bb = tid; bb < B; bb += kThreads) {
+      int sum = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        sum += s_wc[w][bb];
+        s_wc[w][bb] = 0;
+      }
+      s_run[bb] += sum;
+    }
+    __syncthreads();
+  }
+  (void)lane;
+}
+
+// ------------------------------------------------------------------ row gather
+// dst[r] = src[map[r]] for 16-byte-aligned rows; one warp per row, four 16-byte
+// loads in flight per lane.
+__global__ void __launch_bounds__(kThreads)
+gather_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                   const int32_t* __restrict__ map, int nrows, int nsrc, int vec_per_row,
+                   DeviceStatus* st) {
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * kThreads + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * kThreads) >> 5;
+  for (int r = gw; r < nrows; r += nw) {
+    const int s = map[r];
+    uint4* out = dst + (size_t)r * vec_per_row;
+    if ((unsigned)s >= (unsigned)nsrc) {
+      if (lane == 0) record_error(st, kStatusData, kBadPerm, r);
+      for (int v = lane; v < vec_per_row; v += 32) out[v] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const uint4* in = src + (size_t)s * vec_per_row;
+    int v = lane;
+    for (; v + 96 < vec_per_row; v += 128) {
+      const uint4 a = __ldg(in + v), b = __ldg(in + v + 32), c = __ldg(in + v + 64),
+                  d = __ldg(in + v + 96);
+      out[v] = a; out[v + 32] = b; out[v + 64] = c; out[v + 96] = d;
+    }
+    for (; v < vec_per_row; v += 32) out[v] = __ldg(in + v);
+  }
+}
+
+// ------------------------------------------------------------------ LAR
+__device__ __forceinline__ int foe_source(int t, int h, int G, int H) {
+  return H >= G ? (h * G) / H : h * (G / H) + (t % (G / H));
+}
+
+__global__ void __launch_bounds__(kThreads)
+lar_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ src_part,
+           const int32_t* __restrict__ emap, int T, int K, int E, int P, int H,
+           unsigned long long* __restrict__ counts, DeviceStatus* st) {
+  __shared__ int s_map[kMaxBuckets];
+  __shared__ unsigned long long s_red[3][kWarps];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int e = tid; e < E; e += kThreads) {
+    const int p = emap[e];
+    const bool ok = (unsigned)p < (unsigned)P;
+    if (!ok && blockIdx.x == 0) record_error(st, kStatusData, kBadExpertPart, e);
+    s_map[e] = ok ? p : -1;
+  }
+  __syncthreads();
+  unsigned long long loc = 0, base = 0, mx = 0;
+  const int kh = K / H;
+  for (int t = blockIdx.x * kThreads + tid; t < T; t += gridDim.x * kThreads) {
+    int src = -1;
+    if (src_part) {
+      src = src_part[t];
+      if ((unsigned)src >= (unsigned)P) {
+        record_error(st, kStatusData, kBadSrcPart, t);
+        src = -1;
+      }
+    }
+    const int bsrc = (int)(((long long)t * P) / T);
+    const int32_t* row = idx + (size_t)t * K;
+    int best = 0;
+    for (int k = 0; k < K; ++k) {
+      const int e = row[k];
+      int dst = -1;
+      if ((unsigned)e < (unsigned)E) dst = s_map[e];
+      else record_error(st, kStatusData, kBadTopkIdx, (long long)t * K + k);
+      const int sp = src_part ? src : foe_source(t, k / kh, P, H);
+      loc += (dst >= 0 && dst == sp);
+      base += (dst >= 0 && dst == bsrc);
+      if (dst >= 0) {
+        int c = 0;
+        for (int k2 = 0; k2 < K; ++k2) {
+          const int e2 = row[k2];
+          c += ((unsigned)e2 < (unsigned)E && s_map[e2] == dst);
+        }
+        best = max(best, c);
+      }
+    }
+    mx += best;
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) {
+    loc += __shfl_xor_sync(0xffffffffu, loc, off);
+    base += __shfl_xor_sync(0xffffffffu, base, off);
+    mx += __shfl_xor_sync(0xffffffffu, mx, off);
+  }
+  if (lane == 0) { s_red[0][warp] = loc; s_red[1][warp] = base; s_red[2][warp] = mx; }
+  __syncthreads();
+  if (tid < 3) {
+    unsigned long long v = 0;
+    for (int w = 0; w < kWarps; ++w) v += s_red[tid][w];
+    const int slot = tid == 0 ? 0 : (tid == 1 ? 2 : 3);
+    atomicAdd(counts + slot, v);
+  }
+  if (blockIdx.x == 0 && tid == 0) atomicAdd(counts + 1, (unsigned long long)T * K);
+}
+
+int grid_for_rows(long long nrows) {
+  static int sm_count = 0;
+  if (sm_count == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (sm_count <= 0) sm_count = 152;
+  }
+  long long want = (nrows + kWarps - 1) / kWarps;
+  long long cap = (long long)sm_count * 8;
+  return (int)std::max<long long>(1, std::min(want, cap));
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ launchers
+cudaError_t launch_predict_shuffle(const smoe_desc& d, const int32_t* ids, const float* conf,
+                                   const int32_t* emap, const void* x, int32_t* pred,
+                                   int32_t* perm, int32_t* part_off, void* x_shuf, void* ws,
+                                   cudaStream_t s) {
+  WsLayout L;
+  ws_layout(d, &L);
+  DeviceStatus* st = ws_ptr<DeviceStatus>(ws, L.status);
+  int32_t* hist = ws_ptr<int32_t>(ws, L.sort_hist);
+  int32_t* offs = ws_ptr<int32_t>(ws, L.sort_off);
+  const int ntiles = ceil_div(d.T, kSortTile);
+  SMOE_COUNT_LAUNCH(1);
+  predict_hist_kernel<<<ntiles, kThreads, 0, s>>>(ids, conf, emap, d.T, d.E, d.P, d.vocab, pred,
+                                                  hist, ntiles, st);
+  SMOE_COUNT_LAUNCH(1);
+  scan_kernel<<<1, 1024, 0, s>>>(hist, offs, d.P * ntiles, d.P, ntiles, d.T, part_off);
+  SMOE_COUNT_LAUNCH(1);
+  scatter_kernel<kShuffle><<<ntiles, kThreads, 0, s>>>(pred, d.T, d.P, ntiles, offs, perm,
+                                                       nullptr, 0, 0, nullptr, nullptr, nullptr);
+  if (x_shuf) {
+    const int vec = (int)(d.d * elem_size(d) / 16);
+    SMOE_COUNT_LAUNCH(1);
+    gather_rows_kernel<<<grid_for_rows(d.T), kThreads, 0, s>>>(
+        static_cast<const uint4*>(x), static_cast<uint4*>(x_shuf), perm, d.T, d.T, vec, st);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch(const smoe_desc& d, const int32_t* idx, const int32_t* perm,
+                            const void* x_src, int32_t* expert_off, int32_t* pair_row,
+                            int32_t* row_token, void* x_disp, void* ws, cudaStream_t s) {
+  WsLayout L;
+  ws_layout(d, &L);
+  DeviceStatus* st = ws_ptr<DeviceStatus>(ws, L.status);
+  int32_t* hist = ws_ptr<int32_t>(ws, L.sort_hist);
+  int32_t* offs = ws_ptr<int32_t>(ws, L.sort_off);
+  int32_t* row_src = ws_ptr<int32_t>(ws, L.row_src);
+  // the per-pair bucket reuses the row_src slot's twin: pair buckets live after row_src
+  int32_t* bucket = row_src + (size_t)d.T * d.K;
+  const int n = d.T * d.K;
+  const int ntiles = ceil_div(n, kSortTile);
+  SMOE_COUNT_LAUNCH(1);
+  dispatch_hist_kernel<<<ntiles, kThreads, 0, s>>>(idx, perm, d.T, d.K, d.E, bucket, hist, ntiles,
+                                                   st);
+  SMOE_COUNT_LAUNCH(1);
+  scan_kernel<<<1, 1024, 0, s>>>(hist, offs, d.E * ntiles, d.E, ntiles, n, expert_off);
+  SMOE_COUNT_LAUNCH(1);
+  scatter_kernel<kDispatch><<<ntiles, kThreads, 0, s>>>(bucket, n, d.E, ntiles, offs, nullptr,
+                                                        perm, d.T, d.K, pair_row, row_token,
+                                                        row_src);
+  if (x_disp) {
+    const int vec = (int)(d.d * elem_size(d) / 16);
+    SMOE_COUNT_LAUNCH(1);
+    gather_rows_kernel<<<grid_for_rows(n), kThreads, 0, s>>>(
+        static_cast<const uint4*>(x_src), static_cast<uint4*>(x_disp), row_src, n, d.T, vec, st);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lar(const smoe_desc& d, const int32_t* idx, const int32_t* src_part,
+                       const int32_t* emap, unsigned long long* counts, void* ws,
+                       cudaStream_t s) {
+  WsLayout L;
+  ws_layout(d, &L);
+  DeviceStatus* st = ws_ptr<DeviceStatus>(ws, L.status);
+  cudaError_t e = cudaMemsetAsync(counts, 0, 4 * sizeof(unsigned long long), s);
+  if (e != cudaSuccess) return e;
+  const int grid = std::max(1, std::min(ceil_div(d.T, kThreads), 1024));
+  SMOE_COUNT_LAUNCH(1);
+  lar_kernel<<<grid, kThreads, 0, s>>>(idx, src_part, emap, d.T, d.K, d.E, d.P, d.H, counts, st);
+  return cudaGetLastError();
+}
+
+}  // namespace smoe

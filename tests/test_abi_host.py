@@ -1,0 +1,105 @@
+"""The C-ABI library loads without a GPU, exports every declared entry point and
+rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from routing_token_shuffle_gb300 import binding as B
+from routing_token_shuffle_gb300 import build as build_mod
+from routing_token_shuffle_gb300 import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return B.lib()
+
+
+def declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            names.update(re.findall(r"SMOE_API\s+[\w\s\*]+?\b(smoe_\w+)\s*\(", src))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) <= set(B.SIGNATURES), "binding is missing a declared entry point"
+
+
+def test_no_stray_exports(lib):
+    """Only smoe_* symbols are visible (the static CUDA runtime stays local)."""
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    syms = [l.split()[-1] for l in out.splitlines() if l.strip() and " T " in l]
+    assert syms and all(s.startswith("smoe_") for s in syms), syms
+
+
+def test_status_strings(lib):
+    for code in range(-8, 1):
+        assert lib.smoe_status_string(code)
+    assert lib.smoe_status_string(123) == b"unknown status"
+
+
+@pytest.mark.parametrize("name", list(synth.CONFIGS))
+def test_workspace_size_valid_configs(lib, name):
+    d = B.desc_from_config(synth.CONFIGS[name])
+    assert B.workspace_size(d) > 0
+
+
+def base_desc(**kw):
+    d = dict(T=64, d=128, E=8, K=2, H=1, F=256, n_shared=0, P=2, vocab=512, dtype="bf16")
+    d.update(kw)
+    return B.make_desc(**d)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(K=9), -2), (dict(H=3), -2), (dict(K=3, H=2), -2), (dict(E=1024), -2),
+    (dict(K=33, E=64), -2), (dict(P=33), -2), (dict(d=100), -2), (dict(F=12), -2),
+    (dict(T=-1), -2), (dict(n_shared=9), -2), (dict(vocab=0), -2),
+])
+def test_bad_shapes_rejected(lib, kw, code):
+    d = base_desc(**kw)
+    assert lib.smoe_workspace_size(ctypes.byref(d)) == 0
+    rc = lib.smoe_route(ctypes.byref(d), 16, 16, None, 16, 16, 16, None, 0, None)
+    assert rc == code
+    assert lib.smoe_last_error()
+
+
+def test_bad_enum_and_null(lib):
+    d = base_desc()
+    d.dtype = 7
+    assert lib.smoe_route(ctypes.byref(d), 16, 16, None, 16, 16, 16, None, 0, None) == -1
+    d = base_desc()
+    assert lib.smoe_route(ctypes.byref(d), 16, 16, None, 16, None, 16, None, 0, None) == -1
+    assert lib.smoe_route(None, 16, 16, None, 16, 16, 16, None, 0, None) == -1
+
+
+def test_misaligned_pointer_rejected(lib):
+    d = base_desc()
+    assert lib.smoe_route(ctypes.byref(d), 16 + 4, 16, None, 16, 16, 16, None, 0, None) == -3
+
+
+def test_workspace_checks(lib):
+    d = base_desc()
+    n = B.workspace_size(d)
+    args = [ctypes.byref(d), 16, 16, 16, 16, 16, 16, 16, None]
+    assert lib.smoe_predict_shuffle(*args, None, n, None) == -4
+    assert lib.smoe_predict_shuffle(*args, 256 + 16, n, None) == -3
+    assert lib.smoe_predict_shuffle(*args, 256, n - 1, None) == -4
+
+
+def test_grouped_source_rule_needs_divisibility(lib):
+    d = base_desc(E=12, K=3, H=3, P=4)
+    n = B.workspace_size(d)
+    assert lib.smoe_lar(ctypes.byref(d), 16, None, 16, 16, 256, n, None) == -2

@@ -1,0 +1,397 @@
+"""GPU parity: every entry point of the C ABI against the CPU oracle.
+
+Indices, permutations, offsets and counts are compared bit for bit, given the fp32
+logits the GPU exported; values are compared within 2e-2 (max over rows of the
+row's max-abs error over its max-abs reference value). Each workload runs at a
+ragged size the oracle checks in full and at its full size, where values are
+checked on a seeded sample of tokens that includes the last (ragged-tail) token.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import routing_token_shuffle_gb300 as smoe
+from routing_token_shuffle_gb300 import synth
+
+from _cases import Case, rel_err_rows, sample_tokens, to_np
+
+pytestmark = pytest.mark.gpu
+
+VALUE_TOL = 2e-2
+MARGIN = 1e-3
+
+CASES = [("tiny_fp32", None), ("tiny_fp32", 37), ("mixtral", 1001), ("dsv2_prefill", 1537),
+         ("dsv2_decode", None), ("qwen3_foe", 3001),
+         ("mixtral", None), ("dsv2_prefill", None), ("qwen3_foe", None)]
+IDS = [f"{n}-T{t or 'full'}" for n, t in CASES]
+
+_cache = {}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available()
+    yield
+    _cache.clear()
+
+
+def get_case(name, T):
+    key = (name, T)
+    if key not in _cache:
+        if len(_cache) > 2:
+            _cache.clear()
+            torch.cuda.empty_cache()
+        _cache[key] = Case(name, "cuda", T=T)
+    return _cache[key]
+
+
+def i32(*shape):
+    return torch.empty(*shape, dtype=torch.int32, device="cuda")
+
+
+def f32(*shape):
+    return torch.empty(*shape, dtype=torch.float32, device="cuda")
+
+
+def run_route(c, desc, ws):
+    cfg = c.cfg
+    logits, idx, w = f32(cfg.T, cfg.E), i32(cfg.T, cfg.K), f32(cfg.T, cfg.K)
+    smoe.smoe_route(desc, c.x, c.w_gate, idx, w, logits_out=logits, ws=ws)
+    return logits, idx, w
+
+
+@pytest.mark.parametrize("name,T", CASES, ids=IDS)
+def test_route(name, T):
+    c = get_case(name, T)
+    cfg = c.cfg
+    desc = smoe.desc_from_config(cfg)
+    ws = smoe.workspace(desc)
+    logits, idx, w = run_route(c, desc, ws)
+    torch.cuda.synchronize()
+    L = to_np(logits)
+    ref_idx = O.topk_select(L, cfg.K, cfg.H)
+    assert np.array_equal(to_np(idx), ref_idx)
+    np.testing.assert_allclose(to_np(w), O.gate_weights(L, ref_idx), rtol=2e-6, atol=1e-7)
+    rows = sample_tokens(cfg.T, 64)
+    ref_l = O.gate_logits(c.x_np[rows], to_np(c.w_gate))
+    err = np.abs(L[rows] - ref_l).max(axis=1) / np.abs(ref_l).max(axis=1)
+    assert err.max() < 1e-4, err.max()
+    # routing the oracle's logits through logits_in gives the oracle's routes
+    full_ref = O.gate_logits(c.x_np, to_np(c.w_gate)) if cfg.T <= 4096 else None
+    if full_ref is not None:
+        lin = torch.as_tensor(full_ref, device="cuda")
+        idx2, w2 = i32(cfg.T, cfg.K), f32(cfg.T, cfg.K)
+        smoe.smoe_route(desc, None, None, idx2, w2, logits_in=lin, ws=ws)
+        torch.cuda.synchronize()
+        assert np.array_equal(to_np(idx2), O.topk_select(full_ref, cfg.K, cfg.H))
+
+
+@pytest.mark.parametrize("E,K,H", [(8, 2, 1), (160, 6, 1), (128, 8, 8), (64, 8, 2), (512, 32, 1),
+                                   (16, 16, 16), (33 * 3, 3, 3)])
+@pytest.mark.parametrize("renorm", [0, 1])
+def test_route_selection_ties(E, K, H, renorm):
+    """Many exact ties (small-integer logits, +0 and -0): lower index wins."""
+    T = 777
+    rng = np.random.default_rng(E + K + H)
+    vals = np.array([-2.0, -1.0, -0.0, 0.0, 1.0, 3.0], np.float32)
+    L = vals[rng.integers(0, len(vals), size=(T, E))]
+    L[:50] = rng.standard_normal((50, E)).astype(np.float32)
+    desc = smoe.make_desc(T, 64, E, K, H, 64, 0, 2, 100, "bf16", renorm)
+    idx, w = i32(T, K), f32(T, K)
+    smoe.smoe_route(desc, None, None, idx, w, logits_in=torch.as_tensor(L, device="cuda"))
+    torch.cuda.synchronize()
+    ref = O.topk_select(L, K, H)
+    assert np.array_equal(to_np(idx), ref)
+    np.testing.assert_allclose(to_np(w), O.gate_weights(L, ref, renorm=bool(renorm)), rtol=2e-6,
+                               atol=1e-7)
+
+
+def run_shuffle(c, desc, ws, with_x=True):
+    cfg = c.cfg
+    pred, perm, off = i32(cfg.T), i32(cfg.T), i32(cfg.P + 1)
+    xs = torch.empty_like(c.x) if with_x else None
+    smoe.smoe_predict_shuffle(desc, c.ids_d, c.conf_d, c.emap_d, pred, perm, off, ws,
+                              x=c.x if with_x else None, x_shuf=xs)
+    return pred, perm, off, xs
+
+
+@pytest.mark.parametrize("name,T", CASES, ids=IDS)
+def test_predict_shuffle(name, T):
+    c = get_case(name, T)
+    cfg = c.cfg
+    desc = smoe.desc_from_config(cfg)
+    ws = smoe.workspace(desc)
+    pred, perm, off, xs = run_shuffle(c, desc, ws)
+    smoe.smoe_get_status(ws)
+    ref_pred = O.predict_partition(c.ids, c.conf, c.emap, cfg.P)
+    ref_perm, ref_off = O.token_shuffle(ref_pred, cfg.P)
+    assert np.array_equal(to_np(pred), ref_pred)
+    assert np.array_equal(to_np(perm), ref_perm)
+    assert np.array_equal(to_np(off), ref_off)
+    assert torch.equal(xs, c.x[torch.as_tensor(ref_perm, device="cuda").long()])
+
+
+def test_predict_ties_and_empty_partitions():
+    """Rows with exactly tied partition scores and partitions without experts."""
+    V, E, P, T = 64, 12, 5, 3000
+    rng = np.random.default_rng(5)
+    conf = np.full((V, E), 0.25, np.float32)
+    conf[: V // 2] = (rng.integers(0, 9, size=(V // 2, E)) / 8).astype(np.float32)
+    emap = np.array([0, 1, 3, 0, 1, 3, 0, 1, 3, 0, 1, 3], np.int32)   # partitions 2, 4 empty
+    ids = rng.integers(0, V, size=T).astype(np.int32)
+    desc = smoe.make_desc(T, 64, E, 2, 1, 64, 0, P, V, "bf16")
+    ws = smoe.workspace(desc)
+    pred, perm, off = i32(T), i32(T), i32(P + 1)
+    smoe.smoe_predict_shuffle(desc, torch.as_tensor(ids, device="cuda"),
+                              torch.as_tensor(conf, device="cuda"),
+                              torch.as_tensor(emap, device="cuda"), pred, perm, off, ws)
+    smoe.smoe_get_status(ws)
+    ref = O.predict_partition(ids, conf, emap, P)
+    assert np.array_equal(to_np(pred), ref)
+    rp, ro = O.token_shuffle(ref, P)
+    assert np.array_equal(to_np(perm), rp) and np.array_equal(to_np(off), ro)
+
+
+@pytest.mark.parametrize("name,T", CASES, ids=IDS)
+def test_lar(name, T):
+    c = get_case(name, T)
+    cfg = c.cfg
+    desc = smoe.desc_from_config(cfg)
+    ws = smoe.workspace(desc)
+    logits, idx, w = run_route(c, desc, ws)
+    pred, perm, off, _ = run_shuffle(c, desc, ws, with_x=False)
+    counts = torch.empty(4, dtype=torch.int64, device="cuda")
+    smoe.smoe_lar(desc, idx, c.emap_d, counts, ws, src_part=pred)
+    got = to_np(counts).astype(np.uint64)
+    ref = O.lar_counts(to_np(idx), c.emap, cfg.P, cfg.H, src_part=to_np(pred))
+    assert np.array_equal(got, ref)
+    if cfg.P % cfg.H == 0 or cfg.H >= cfg.P:
+        foe_map = synth.placement_foe(cfg.E, cfg.H, cfg.P)
+        smoe.smoe_lar(desc, idx, torch.as_tensor(foe_map, device="cuda"), counts, ws)
+        ref2 = O.lar_counts(to_np(idx), foe_map, cfg.P, cfg.H)
+        assert np.array_equal(to_np(counts).astype(np.uint64), ref2)
+        if cfg.H >= cfg.P:
+            assert ref2[0] == ref2[1]           # rho_foe = min(H/G, 1) = 1
+    smoe.smoe_get_status(ws)
+
+
+@pytest.mark.parametrize("name,T", CASES, ids=IDS)
+def test_dispatch(name, T):
+    c = get_case(name, T)
+    cfg = c.cfg
+    desc = smoe.desc_from_config(cfg)
+    ws = smoe.workspace(desc)
+    logits, idx, w = run_route(c, desc, ws)
+    pred, perm, off, xs = run_shuffle(c, desc, ws)
+    TK = cfg.T * cfg.K
+    eo, pr, rt = i32(cfg.E + 1), i32(cfg.T, cfg.K), i32(TK)
+    xd = torch.empty(TK, cfg.d, dtype=c.x.dtype, device="cuda")
+    smoe.smoe_dispatch(desc, idx, eo, pr, rt, ws, shuf_perm=perm, x_src=xs, x_disp=xd)
+    smoe.smoe_get_status(ws)
+    r_eo, r_pr, r_rt = O.expert_dispatch(to_np(idx), cfg.E, to_np(perm))
+    assert np.array_equal(to_np(eo), r_eo)
+    assert np.array_equal(to_np(pr), r_pr)
+    assert np.array_equal(to_np(rt), r_rt)
+    assert torch.equal(xd, c.x[torch.as_tensor(r_rt, device="cuda").long()])
+    # without the shuffle: token order, source rows straight from x
+    smoe.smoe_dispatch(desc, idx, eo, pr, rt, ws, x_src=c.x, x_disp=xd)
+    smoe.smoe_get_status(ws)
+    r_eo, r_pr, r_rt = O.expert_dispatch(to_np(idx), cfg.E, None)
+    assert np.array_equal(to_np(pr), r_pr) and np.array_equal(to_np(rt), r_rt)
+    assert torch.equal(xd, c.x[torch.as_tensor(r_rt, device="cuda").long()])
+
+
+@pytest.mark.parametrize("name,T", CASES, ids=IDS)
+def test_expert_ffn_and_combine(name, T):
+    c = get_case(name, T)
+    cfg = c.cfg
+    desc = smoe.desc_from_config(cfg)
+    ws = smoe.workspace(desc)
+    logits, idx, w = run_route(c, desc, ws)
+    TK = cfg.T * cfg.K
+    eo, pr, rt = i32(cfg.E + 1), i32(cfg.T, cfg.K), i32(TK)
+    xd = torch.empty(TK, cfg.d, dtype=c.x.dtype, device="cuda")
+    smoe.smoe_dispatch(desc, idx, eo, pr, rt, ws, x_src=c.x, x_disp=xd)
+    yd = torch.empty_like(xd)
+    ysh = (torch.empty(cfg.n_shared, cfg.T, cfg.d, dtype=c.x.dtype, device="cuda")
+           if cfg.n_shared else None)
+    smoe.smoe_expert_ffn(desc, xd, eo, c.w1, c.w3, c.w2, yd, ws, x=c.x, y_shared=ysh)
+    y = torch.empty_like(c.x)
+    smoe.smoe_combine(desc, yd, pr, w, y, ws, y_shared=ysh)
+    smoe.smoe_get_status(ws)
+    torch.cuda.synchronize()
+    # expert outputs on sampled rows (the last row of every expert segment included)
+    eo_n, rt_n, idx_n = to_np(eo), to_np(rt), to_np(idx)
+    rows = set(sample_tokens(TK, 48, seed=1).tolist())
+    rows.update(int(eo_n[e + 1] - 1) for e in range(cfg.E) if eo_n[e + 1] > eo_n[e])
+    rows = np.array(sorted(rows))
+    row_exp = np.searchsorted(eo_n, rows, side="right") - 1
+    ref = np.zeros((len(rows), cfg.d))
+    for e in np.unique(row_exp):
+        sel = row_exp == e
+        ref[sel] = O.swiglu_ffn(c.x_np[rt_n[rows[sel]]], *c.expert_weights_np(int(e)))
+    assert rel_err_rows(to_np(yd)[rows], ref).max() <= VALUE_TOL
+    if cfg.n_shared:
+        toks = sample_tokens(cfg.T, 16, seed=2)
+        for j in range(cfg.n_shared):
+            rj = O.swiglu_ffn(c.x_np[toks], *c.expert_weights_np(cfg.E + j))
+            assert rel_err_rows(to_np(ysh[j])[toks], rj).max() <= VALUE_TOL
+    # combine against the oracle's combine of the GPU's own expert outputs
+    toks = sample_tokens(cfg.T, 256, seed=3)
+    y_rows = to_np(yd)
+    ysh_n = to_np(ysh)[:, toks] if cfg.n_shared else None
+    ref_y = O.combine(y_rows, to_np(pr)[toks], to_np(w)[toks], ysh_n)
+    tol = 1e-5 if cfg.dtype == "f32" else 8e-3
+    assert rel_err_rows(to_np(y)[toks], ref_y).max() <= tol
+
+
+@pytest.mark.parametrize("name,T", CASES, ids=IDS)
+def test_layer_forward(name, T):
+    c = get_case(name, T)
+    cfg = c.cfg
+    desc = smoe.desc_from_config(cfg)
+    ws = smoe.workspace(desc)
+    TK = cfg.T * cfg.K
+    outs = dict(logits=f32(cfg.T, cfg.E), topk_idx=i32(cfg.T, cfg.K), topk_w=f32(cfg.T, cfg.K),
+                pred_part=i32(cfg.T), shuf_perm=i32(cfg.T), part_off=i32(cfg.P + 1),
+                expert_off=i32(cfg.E + 1), pair_row=i32(cfg.T, cfg.K), row_token=i32(TK),
+                lar=torch.empty(4, dtype=torch.int64, device="cuda"))
+    y = torch.empty_like(c.x)
+    W = smoe.layer_weights(c.w_gate, c.w1, c.w3, c.w2, c.conf_d, c.emap_d)
+    smoe.smoe_layer_forward(desc, W, smoe.layer_io(c.x, c.ids_d, y, **outs), ws)
+    smoe.smoe_get_status(ws)
+    torch.cuda.synchronize()
+    L = to_np(outs["logits"])
+    idx = O.topk_select(L, cfg.K, cfg.H)
+    assert np.array_equal(to_np(outs["topk_idx"]), idx)
+    pred = O.predict_partition(c.ids, c.conf, c.emap, cfg.P)
+    perm, off = O.token_shuffle(pred, cfg.P)
+    eo, pr, rt = O.expert_dispatch(idx, cfg.E, perm)
+    for k, ref in (("pred_part", pred), ("shuf_perm", perm), ("part_off", off),
+                   ("expert_off", eo), ("pair_row", pr), ("row_token", rt)):
+        assert np.array_equal(to_np(outs[k]), ref), k
+    assert np.array_equal(to_np(outs["lar"]).astype(np.uint64),
+                          O.lar_counts(idx, c.emap, cfg.P, cfg.H, src_part=pred))
+    # values against the oracle's own routing, tokens near a routing tie excluded
+    toks = np.arange(cfg.T) if cfg.T <= 1024 else sample_tokens(cfg.T, 40, seed=4)
+    own_logits = O.gate_logits(c.x_np[toks], to_np(c.w_gate))
+    margin = O.selection_margin(own_logits, cfg.K, cfg.H)
+    keep = margin >= MARGIN
+    assert keep.mean() > 0.8
+    own_idx = np.zeros((cfg.T, cfg.K), np.int64)
+    own_w = np.zeros((cfg.T, cfg.K))
+    own_idx[toks] = O.topk_select(own_logits, cfg.K, cfg.H)
+    own_w[toks] = O.gate_weights(own_logits, own_idx[toks])
+    ref = c.oracle_tokens(toks[keep], own_idx, own_w)
+    err = rel_err_rows(to_np(y)[toks[keep]], ref)
+    assert err.max() <= VALUE_TOL, err.max()
+
+
+def test_layer_forward_host_buffers():
+    c = get_case("tiny_fp32", None)
+    cfg = c.cfg
+    desc = smoe.desc_from_config(cfg)
+    ws = smoe.workspace(desc)
+    W = smoe.layer_weights(c.w_gate, c.w1, c.w3, c.w2, c.conf_d, c.emap_d)
+    y_dev = torch.empty_like(c.x)
+    smoe.smoe_layer_forward(desc, W, smoe.layer_io(c.x, c.ids_d, y_dev), ws)
+    xh = c.x.cpu().pin_memory()
+    ih = torch.as_tensor(c.ids).pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    smoe.smoe_layer_forward_host(desc, W, xh, ih, yh, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(yh, y_dev.cpu())
+
+
+def test_skip_shuffle_is_lossless():
+    """Dispatching without the shuffle gives the same output (the shuffle only moves
+    data: the pages call s-MoE lossless)."""
+    c = get_case("qwen3_foe", 3001)
+    cfg = c.cfg
+    desc = smoe.desc_from_config(cfg)
+    ws = smoe.workspace(desc)
+    W = smoe.layer_weights(c.w_gate, c.w1, c.w3, c.w2, c.conf_d, c.emap_d)
+    y1, y2 = torch.empty_like(c.x), torch.empty_like(c.x)
+    smoe.smoe_layer_forward(desc, W, smoe.layer_io(c.x, c.ids_d, y1), ws)
+    smoe.smoe_layer_forward(desc, W, smoe.layer_io(c.x, c.ids_d, y2, skip_shuffle=1), ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+
+
+@pytest.mark.parametrize("T", [3001, None])
+def test_prefetch_predict(T):
+    c = get_case("qwen3_foe", T)
+    cfg = c.cfg
+    desc = smoe.desc_from_config(cfg)
+    ws = smoe.workspace(desc)
+    r, wgn, gamma, beta = synth.predictor_inputs(cfg, "cuda")
+    wgn_l = wgn.to(cfg.torch_dtype)
+    d_l = synth.round_bf16(torch.randn(cfg.d, device="cuda", generator=torch.Generator(
+        device="cuda").manual_seed(11)) * 0.3)
+    W = smoe.layer_weights(c.w_gate, c.w1, c.w3, c.w2, c.conf_d, c.emap_d)
+    y = torch.empty_like(c.x)
+    smoe.smoe_layer_forward(desc, W, smoe.layer_io(c.x, c.ids_d, y), ws)
+    lq, ls = f32(cfg.T, cfg.E), f32(cfg.T, cfg.E)
+    pi, ti = i32(cfg.T, cfg.K), i32(cfg.T, cfg.K)
+    hits = torch.empty(1, dtype=torch.int64, device="cuda")
+    smoe.smoe_prefetch_predict(desc, r, d_l, y, gamma, beta, wgn_l, pi, ti, hits, ws,
+                               logits_q=lq, logits_s=ls)
+    smoe.smoe_get_status(ws)
+    torch.cuda.synchronize()
+    Lq, Ls = to_np(lq), to_np(ls)
+    rp, rtru = O.topk_select(Lq, cfg.K, cfg.H), O.topk_select(Ls, cfg.K, cfg.H)
+    assert np.array_equal(to_np(pi), rp) and np.array_equal(to_np(ti), rtru)
+    assert int(to_np(hits)[0]) == O.hit_count(rp, rtru)
+    toks = sample_tokens(cfg.T, 64, seed=5)
+    ref = O.prefetch_predict(to_np(r)[toks], to_np(d_l), to_np(y)[toks], to_np(gamma),
+                             to_np(beta), to_np(wgn_l), cfg.K, cfg.H)
+    assert rel_err_rows(Lq[toks], ref["logits_q"]).max() <= VALUE_TOL
+    assert rel_err_rows(Ls[toks], ref["logits_s"]).max() <= VALUE_TOL
+    # y rows equal to the default vector: every prediction is a hit
+    y_eq = d_l.to(cfg.torch_dtype).expand(cfg.T, cfg.d).contiguous()
+    smoe.smoe_prefetch_predict(desc, r, d_l, y_eq, gamma, beta, wgn_l, pi, ti, hits, ws)
+    torch.cuda.synchronize()
+    assert int(to_np(hits)[0]) == cfg.T * cfg.K
+
+
+def test_out_of_range_data_is_reported_and_skipped():
+    c = get_case("tiny_fp32", None)
+    cfg = c.cfg
+    desc = smoe.desc_from_config(cfg)
+    ws = smoe.workspace(desc)
+    bad = c.ids_d.clone()
+    bad[5] = cfg.vocab + 3
+    pred, perm, off = i32(cfg.T), i32(cfg.T), i32(cfg.P + 1)
+    smoe.smoe_predict_shuffle(desc, bad, c.conf_d, c.emap_d, pred, perm, off, ws)
+    with pytest.raises(smoe.SmoeError) as ei:
+        smoe.smoe_get_status(ws)
+    assert ei.value.code == -6
+    ref = O.predict_partition(c.ids, c.conf, c.emap, cfg.P)
+    got = to_np(pred)
+    assert got[5] == 0 and np.array_equal(np.delete(got, 5), np.delete(ref, 5))
+    smoe.smoe_get_status(ws)          # cleared
+    idx = i32(cfg.T, cfg.K)
+    idx.fill_(1)
+    idx[3, 1] = cfg.E + 10
+    eo, pr, rt = i32(cfg.E + 1), i32(cfg.T, cfg.K), i32(cfg.T * cfg.K)
+    smoe.smoe_dispatch(desc, idx, eo, pr, rt, ws)
+    with pytest.raises(smoe.SmoeError):
+        smoe.smoe_get_status(ws)
+
+
+def test_empty_batch():
+    desc = smoe.make_desc(0, 128, 8, 2, 1, 256, 0, 2, 512, "f32")
+    ws = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    ws_n = smoe.workspace_size(desc)
+    ws = torch.zeros(max(ws_n, 256), dtype=torch.uint8, device="cuda")
+    off = torch.full((3,), 7, dtype=torch.int32, device="cuda")
+    e = torch.empty(0, dtype=torch.int32, device="cuda")
+    conf = torch.zeros(512, 8, device="cuda")
+    emap = torch.zeros(8, dtype=torch.int32, device="cuda")
+    smoe.smoe_predict_shuffle(desc, conf, conf, emap, conf, conf, off, ws)
+    torch.cuda.synchronize()
+    assert to_np(off).tolist() == [0, 0, 0]
+    del e
