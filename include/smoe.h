@@ -125,6 +125,28 @@ SMOE_API int smoe_predict_shuffle(const smoe_desc* desc, const int32_t* token_id
                                   int32_t* pred_part, int32_t* shuf_perm, int32_t* part_off,
                                   void* x_shuf, void* ws, size_t ws_bytes, void* stream);
 
+/* Workspace-free variant of smoe_predict_shuffle, for callers that cannot allocate
+ * device memory: code running while a CUDA graph is being captured (where allocation
+ * calls are not allowed), runtimes that forbid allocation after start-up, or hosts
+ * whose device memory pool belongs to another framework. The pages have no
+ * counterpart; it computes exactly what smoe_predict_shuffle computes, with the same
+ * arguments minus the workspace.
+ *   - Its histogram scratch is a 256 KB array inside the library that every GPU which
+ *     loads the library holds until the process exits; T is limited to 1048576 tokens
+ *     (1024 tiles of 1024), larger T returns SMOE_ERR_SHAPE.
+ *   - It allocates nothing and calls no allocating routine.
+ *   - The first call on a device looks up that array's device address (with the
+ *     device current); make that first call before any stream capture begins.
+ *   - All calls share the one array: calls that overlap on the GPU (different
+ *     streams, or different host threads) race and must be serialised by the caller.
+ *     Every call rewrites the parts it reads, so nothing carries over between calls.
+ *   - Device data errors are not reported (there is no status word): an out-of-range
+ *     token id or map entry gives partition 0, as in smoe_predict_shuffle.          */
+SMOE_API int smoe_predict_shuffle_noalloc(const smoe_desc* desc, const int32_t* token_ids,
+                                          const float* conf, const int32_t* expert_part,
+                                          const void* x, int32_t* pred_part, int32_t* shuf_perm,
+                                          int32_t* part_off, void* x_shuf, void* stream);
+
 /* a5 -- local activation rate counts ("Speculative MoE" §2/§7: the fraction of
  * routed (token, expert) pairs whose expert sits on the token's device; FoE:
  * rho_moe = 1/G, rho_foe = min(H/G, 1)).

@@ -52,6 +52,7 @@ SIGNATURES = {
     "smoe_workspace_size": (_SZ, [_D]),
     "smoe_route": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "smoe_predict_shuffle": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "smoe_predict_shuffle_noalloc": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "smoe_lar": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _SZ, _P]),
     "smoe_dispatch": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "smoe_expert_ffn": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -145,6 +146,15 @@ def smoe_predict_shuffle(desc, token_ids, conf, expert_part, pred_part, shuf_per
                                       _ptr(expert_part), _ptr(x), _ptr(pred_part), _ptr(shuf_perm),
                                       _ptr(part_off), _ptr(x_shuf), _ptr(ws), ws.numel(),
                                       _stream(stream)), "smoe_predict_shuffle")
+
+
+def smoe_predict_shuffle_noalloc(desc, token_ids, conf, expert_part, pred_part, shuf_perm,
+                                 part_off, x=None, x_shuf=None, stream=None):
+    """smoe_predict_shuffle without a workspace (library-held scratch; see smoe.h)."""
+    _check(lib().smoe_predict_shuffle_noalloc(ctypes.byref(desc), _ptr(token_ids), _ptr(conf),
+                                              _ptr(expert_part), _ptr(x), _ptr(pred_part),
+                                              _ptr(shuf_perm), _ptr(part_off), _ptr(x_shuf),
+                                              _stream(stream)), "smoe_predict_shuffle_noalloc")
 
 
 def smoe_lar(desc, topk_idx, expert_part, counts, ws, src_part=None, stream=None):

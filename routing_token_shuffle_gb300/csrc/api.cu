@@ -90,6 +90,8 @@ int check_ws(const smoe_desc* d, void* ws, size_t ws_bytes) {
 
 }  // namespace
 
+int set_last_error(int code, const char* msg) { return fail(code, "%s", msg); }
+
 int check_desc(const smoe_desc* d) {
   SMOE_REQUIRE(d != nullptr, SMOE_ERR_ARG, "desc must not be NULL");
   SMOE_REQUIRE(d->dtype == SMOE_F32 || d->dtype == SMOE_BF16, SMOE_ERR_ARG, "bad dtype %d", d->dtype);

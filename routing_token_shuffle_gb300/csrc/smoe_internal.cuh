@@ -95,6 +95,7 @@ constexpr int kSortTile = 1024;     // elements per counting-sort tile
 constexpr int kMaxGroups = 520;     // E + n_shared upper bound
 
 bool ws_layout(const smoe_desc& d, WsLayout* out);
+int set_last_error(int code, const char* msg);  // records msg for smoe_last_error, returns code
 int check_desc(const smoe_desc* d);  // smoe_status
 
 inline size_t elem_size(const smoe_desc& d) { return d.dtype == SMOE_F32 ? 4 : 2; }

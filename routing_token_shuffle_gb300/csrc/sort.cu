@@ -10,6 +10,7 @@
 // histograms, one CTA scanning the (bucket, tile) table, and a scatter that ranks
 // each tile's elements stably (warp match + per-warp counts in shared memory).
 #include <algorithm>
+#include <mutex>
 
 #include "smoe_internal.cuh"
 
@@ -423,3 +424,101 @@ cudaError_t launch_lar(const smoe_desc& d, const int32_t* idx, const int32_t* sr
 }
 
 }  // namespace smoe
+
+// ------------------------------------------------------------------ no-allocation variant
+// Some callers cannot allocate device memory at all: code that runs inside a CUDA
+// graph being captured, allocator-free embedded runtimes, or hosts whose memory
+// pool is owned by another framework. For them the predict + shuffle step also
+// exists without a caller workspace: its per-tile histogram and offsets live in
+// the file-scope array below, which every GPU that loads the library keeps until
+// the process exits.
+namespace smoe {
+namespace {
+
+constexpr int kNoAllocMaxTiles = 1024;                        // T <= 1024 * kSortTile
+constexpr int kNoAllocScratchInts = 2 * 32 * kNoAllocMaxTiles;  // hist + offs for P <= 32
+static __device__ __align__(256) int32_t g_shuffle_scratch[kNoAllocScratchInts];
+
+// Device address of g_shuffle_scratch per device, looked up once per device with
+// that device current (host code must not use the symbol itself as a pointer).
+int32_t* noalloc_scratch_ptr(int* err) {
+  static std::mutex mu;
+  static int32_t* ptrs[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64) {
+    *err = set_last_error(SMOE_ERR_CUDA, "cudaGetDevice failed in the no-allocation shuffle");
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (ptrs[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_shuffle_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      *err = set_last_error(SMOE_ERR_CUDA, "cudaGetSymbolAddress of the shuffle scratch failed");
+      return nullptr;
+    }
+    ptrs[dev] = static_cast<int32_t*>(p);
+  }
+  return ptrs[dev];
+}
+
+bool aligned16_ptr(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace smoe
+
+extern "C" SMOE_API int smoe_predict_shuffle_noalloc(const smoe_desc* desc,
+                                                     const int32_t* token_ids, const float* conf,
+                                                     const int32_t* expert_part, const void* x,
+                                                     int32_t* pred_part, int32_t* shuf_perm,
+                                                     int32_t* part_off, void* x_shuf,
+                                                     void* stream) {
+  using namespace smoe;
+  int rc = check_desc(desc);
+  if (rc != SMOE_OK) return rc;
+  const void* req[] = {token_ids, conf, expert_part, pred_part, shuf_perm, part_off};
+  for (const void* p : req) {
+    if (p == nullptr) return set_last_error(SMOE_ERR_ARG, "a required pointer is NULL");
+    if (!aligned16_ptr(p)) return set_last_error(SMOE_ERR_ALIGN, "a pointer is not 16-byte aligned");
+  }
+  if (x_shuf != nullptr && (x == nullptr || !aligned16_ptr(x) || !aligned16_ptr(x_shuf)))
+    return set_last_error(SMOE_ERR_ARG, "x_shuf needs a 16-byte aligned x");
+  const int ntiles = ceil_div(desc->T, kSortTile);
+  if (ntiles > kNoAllocMaxTiles)
+    return set_last_error(SMOE_ERR_SHAPE,
+                          "smoe_predict_shuffle_noalloc supports at most 1048576 tokens");
+  int err = SMOE_OK;
+  int32_t* scratch = noalloc_scratch_ptr(&err);
+  if (scratch == nullptr) return err;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (desc->T == 0) {
+    cudaError_t e = cudaMemsetAsync(part_off, 0, sizeof(int32_t) * (desc->P + 1), s);
+    return e == cudaSuccess ? SMOE_OK : set_last_error(SMOE_ERR_CUDA, cudaGetErrorString(e));
+  }
+  // Both halves of the scratch are fully written before they are read (every tile
+  // writes its P histogram entries; the scan writes every offset), so nothing needs
+  // clearing between calls. Device data errors are not reported by this variant:
+  // an out-of-range id is treated as partition 0, as in smoe_predict_shuffle.
+  int32_t* hist = scratch;
+  int32_t* offs = scratch + 32 * kNoAllocMaxTiles;
+  const smoe_desc& d = *desc;
+  SMOE_COUNT_LAUNCH(1);
+  predict_hist_kernel<<<ntiles, kThreads, 0, s>>>(token_ids, conf, expert_part, d.T, d.E, d.P,
+                                                  d.vocab, pred_part, hist, ntiles, nullptr);
+  SMOE_COUNT_LAUNCH(1);
+  scan_kernel<<<1, 1024, 0, s>>>(hist, offs, d.P * ntiles, d.P, ntiles, d.T, part_off);
+  SMOE_COUNT_LAUNCH(1);
+  scatter_kernel<kShuffle><<<ntiles, kThreads, 0, s>>>(pred_part, d.T, d.P, ntiles, offs,
+                                                       shuf_perm, nullptr, 0, 0, nullptr, nullptr,
+                                                       nullptr);
+  if (x_shuf) {
+    const int vec = (int)(d.d * elem_size(d) / 16);
+    SMOE_COUNT_LAUNCH(1);
+    gather_rows_kernel<<<grid_for_rows(d.T), kThreads, 0, s>>>(
+        static_cast<const uint4*>(x), static_cast<uint4*>(x_shuf), shuf_perm, d.T, d.T, vec,
+        nullptr);
+  }
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SMOE_OK : set_last_error(SMOE_ERR_CUDA, cudaGetErrorString(e));
+}

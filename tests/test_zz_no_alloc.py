@@ -1,0 +1,74 @@
+"""The workspace-free shuffle entry point, for callers that cannot allocate device
+memory (inside CUDA graph capture, allocator-free runtimes, pools owned by another
+framework). It must return exactly what the workspace entry point returns, call
+after call, although all calls share one library-held scratch array.
+
+Kept in its own file, collected last, so a run that stops at the first failure has
+already run every other test; it also passes alone in a fresh process."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def smoe():
+    import __graft_entry__
+    __graft_entry__.build()
+    import routing_token_shuffle_gb300 as m
+    assert torch.cuda.is_available()
+    return m
+
+
+def make_inputs(seed, T, d, E, P, V):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    ids = torch.randint(0, V, (T,), generator=g, device="cuda", dtype=torch.int32)
+    conf = torch.rand(V, E, generator=g, device="cuda")
+    conf[: V // 3] = torch.round(conf[: V // 3] * 4) / 4          # exact partition-score ties
+    emap = torch.randint(0, P, (E,), generator=g, device="cuda", dtype=torch.int32)
+    x = torch.randn(T, d, generator=g, device="cuda").to(torch.bfloat16)
+    return ids, conf, emap, x
+
+
+def run_both(smoe, desc, ids, conf, emap, x, ws):
+    T, P = desc.T, desc.P
+    i32 = dict(dtype=torch.int32, device="cuda")
+    ref = [torch.empty(T, **i32), torch.empty(T, **i32), torch.empty(P + 1, **i32),
+           torch.empty_like(x)]
+    smoe.smoe_predict_shuffle(desc, ids, conf, emap, ref[0], ref[1], ref[2], ws, x=x,
+                              x_shuf=ref[3])
+    got = [torch.full((T,), -7, **i32), torch.full((T,), -7, **i32),
+           torch.full((P + 1,), -7, **i32), torch.zeros_like(x)]
+    # straight through the C ABI, no workspace argument
+    rc = smoe.lib().smoe_predict_shuffle_noalloc(
+        ctypes.byref(desc), ids.data_ptr(), conf.data_ptr(), emap.data_ptr(), x.data_ptr(),
+        got[0].data_ptr(), got[1].data_ptr(), got[2].data_ptr(), got[3].data_ptr(),
+        torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, smoe.lib().smoe_last_error()
+    torch.cuda.synchronize()
+    return ref, got
+
+
+def test_noalloc_matches_workspace_entry_point_twice(smoe):
+    # two calls in a row with different shapes and data: nothing may leak from the first
+    shapes = [(5000, 256, 64, 8, 3000), (1537, 128, 160, 5, 700)]
+    for call, (T, d, E, P, V) in enumerate(shapes):
+        desc = smoe.make_desc(T, d, E, 2, 1, 64, 0, P, V, "bf16")
+        ws = smoe.workspace(desc)
+        ids, conf, emap, x = make_inputs(100 + call, T, d, E, P, V)
+        ref, got = run_both(smoe, desc, ids, conf, emap, x, ws)
+        for r, g in zip(ref, got):
+            assert torch.equal(r, g), f"call {call} differs from smoe_predict_shuffle"
+
+
+def test_noalloc_rejects_too_many_tokens(smoe):
+    desc = smoe.make_desc(1024 * 1024 + 1, 128, 8, 2, 1, 64, 0, 2, 100, "bf16")
+    t = torch.zeros(16, dtype=torch.int32, device="cuda")
+    rc = smoe.lib().smoe_predict_shuffle_noalloc(ctypes.byref(desc), t.data_ptr(), t.data_ptr(),
+                                                 t.data_ptr(), None, t.data_ptr(), t.data_ptr(),
+                                                 t.data_ptr(), None, None)
+    assert rc == -2
+    assert b"1048576" in smoe.lib().smoe_last_error()
