@@ -1,17 +1,45 @@
-// Grouped SwiGLU expert FFN over the expert-contiguous rows written by dispatch.
+// Grouped SwiGLU expert FFN on the 5th-generation tensor cores (tcgen05 + TMEM +
+// TMA), over the expert-contiguous rows written by dispatch.
 //
 // Group g < E is routed expert g (rows expert_off[g] .. expert_off[g+1] of x_disp);
-// group E + j is shared expert j, run on all T rows of x. The up projection writes
-// H = silu(A W1^T) * (A W3^T) rounded to the element type; the down projection
-// writes Y = H W2^T.
-#include "smoe_internal.cuh"
+// group E + j is shared expert j, run on all T rows of x. Two launches:
+//   up:   H[r, n]  = silu(A W1^T)[r, n] * (A W3^T)[r, n]   (H rounded to the element type)
+//   down: Y[r, n]  = (H W2^T)[r, n]
+// Each is a persistent kernel, one CTA per SM, walking a tile list (group, n-tile,
+// m-tile) with m fastest so that the CTAs working at the same time share weight
+// tiles through L2. Inside a CTA:
+//   warp 0  one thread issues TMA loads into a 4-stage shared-memory ring
+//           (stage = A 128 x 128 B + B 256 x 128 B, 128-byte swizzle);
+//   warp 1  one thread issues tcgen05.mma (M = 128, N = 256, K = 16 bf16 / 8 tf32)
+//           into one of two TMEM accumulators of 256 fp32 columns;
+//   warp 2  allocates and frees the 512 TMEM columns;
+//   warps 4-7 drain an accumulator (tcgen05.ld, one TMEM lane = one row per thread),
+//           apply SwiGLU (up) and store, while the MMAs of the next tile run.
+// In the up GEMM the B stage holds 128 rows of W1 followed by the same 128 rows of
+// W3, so one N = 256 MMA produces the gate and up halves of the tile together.
+// Expert segments are not padded: a tile reaching past its group's last row reads
+// the following rows (or TMA's zero fill) and its stores are masked.
+#include <algorithm>
+#include <mutex>
+#include <type_traits>
+
+#include "tc_common.cuh"
 
 namespace smoe {
 namespace {
 
-// tile_start[g] = first tile of group g for a row-tile height bm; tile_start[G] = total.
-// expert_off must be non-decreasing from 0 to at most T K; otherwise no tile is
-// scheduled and the status word records the error.
+constexpr int kBM = 128;
+constexpr int kStages = 4;
+constexpr uint32_t kStageA = 128 * 128;  // 128 rows x 128 bytes
+constexpr uint32_t kStageB = 256 * 128;  // 256 rows x 128 bytes
+constexpr int kThreads = 256;
+constexpr int kAccCols = 256;            // fp32 columns per accumulator
+constexpr size_t kSmemBytes =
+    1024 + kStages * (kStageA + kStageB) + 256 + 4 * (kMaxGroups + 1 + 513 + 4);
+
+// tile_start[g] = first m-tile of group g; tile_start[G] = total m-tiles. expert_off must
+// be non-decreasing from 0 to at most T K; otherwise no tile is scheduled and the status
+// word records the error.
 __global__ void tile_table_kernel(const int32_t* __restrict__ expert_off, int E, int n_shared,
                                   int T, int TK, int bm, int32_t* __restrict__ tile_start,
                                   DeviceStatus* st) {
@@ -47,137 +75,370 @@ __global__ void tile_table_kernel(const int32_t* __restrict__ expert_off, int E,
   if (lane == 0) tile_start[G] = carry;
 }
 
-struct GroupRows {
-  int g, m0, rows;   // group, first row of this tile within the group, rows in the group
+struct GemmArgs {
+  const int32_t* expert_off;  // [E+1]
+  const int32_t* tile_start;  // [G+1] m-tiles per group, prefix
+  void* out;                  // up: H [TK + S T, F]; down: y_disp [TK, d]
+  void* out_sh;               // down: y_shared [S, T, d]
+  DeviceStatus* st;
+  int E, G, T, TK;
+  int N;                      // output columns: F (up) or d (down)
+  int KD;                     // contraction length: d (up) or F (down)
+  int NT;                     // n-tiles
 };
 
-__device__ __forceinline__ bool find_tile(const int32_t* tile_start, int G, int tile, int bm,
-                                          const int32_t* expert_off, int E, int T, GroupRows* out) {
-  if (tile >= tile_start[G]) return false;
-  int lo = 0, hi = G - 1;
-  while (lo < hi) {  // last g with tile_start[g] <= tile
+struct Tile {
+  int g, m0, n0, rows;
+  int a_row;          // first A row in its tensor map
+  bool a_shared;      // A from the shared-input map (x) instead of the routed map
+  int b_row;          // first B row
+  long long out_row;  // first output row (in out, or in out_sh for a shared down tile)
+  bool out_shared;
+};
+
+template <bool UP>
+__device__ __forceinline__ void decode_tile(const int32_t* ts, const int32_t* eo,
+                                            const GemmArgs& p, int t, Tile& r) {
+  int lo = 0, hi = p.G - 1;
+  while (lo < hi) {  // largest g whose first tile is <= t (empty groups are skipped)
     const int mid = (lo + hi + 1) >> 1;
-    if (tile_start[mid] <= tile) lo = mid; else hi = mid - 1;
+    if (ts[mid] * p.NT <= t) lo = mid; else hi = mid - 1;
   }
-  out->g = lo;
-  out->m0 = (tile - tile_start[lo]) * bm;
-  out->rows = lo < E ? expert_off[lo + 1] - expert_off[lo] : T;
-  return true;
-}
-
-constexpr int kBM = 64, kBN = 64, kBK = 16;
-
-// SIMT reference-speed grouped GEMM: 64x64 output tile per CTA, fp32 FMA.
-// UP: out = H rows, computes both W1 and W3 tiles and applies SwiGLU.
-template <typename TE, bool UP>
-__global__ void __launch_bounds__(256)
-ffn_simt_kernel(const TE* __restrict__ a_routed, const TE* __restrict__ a_shared,
-                const int32_t* __restrict__ expert_off, const int32_t* __restrict__ tile_start,
-                const TE* __restrict__ wa, const TE* __restrict__ wb, TE* __restrict__ out_routed,
-                TE* __restrict__ out_shared, int E, int n_shared, int T, int TK, int N, int KD) {
-  __shared__ float as[kBK][kBM + 4];
-  __shared__ float b1s[kBK][kBN + 4];
-  __shared__ float b3s[kBK][UP ? kBN + 4 : 1];
-  GroupRows gr;
-  if (!find_tile(tile_start, E + n_shared, blockIdx.x, kBM, expert_off, E, T, &gr)) return;
-  const int n0 = blockIdx.y * kBN;
-  const bool shared = gr.g >= E;
-  const int j = gr.g - E;
-  // A rows and output rows of this group
-  const TE* A;
-  TE* O;
+  const int g = lo;
+  const int mt = ts[g + 1] - ts[g];
+  const int local = t - ts[g] * p.NT;
+  const int n_tile = local / mt, m_tile = local - n_tile * mt;
+  r.g = g;
+  r.m0 = m_tile * kBM;
+  const bool shared = g >= p.E;
+  const int j = g - p.E;
+  r.rows = shared ? p.T : eo[g + 1] - eo[g];
   if (UP) {
-    A = shared ? a_shared : a_routed + (size_t)expert_off[gr.g] * KD;
-    O = out_routed + (size_t)(shared ? TK + j * T : expert_off[gr.g]) * N;  // H buffer
+    r.n0 = n_tile * 128;
+    r.a_shared = shared;
+    r.a_row = (shared ? 0 : eo[g]) + r.m0;
+    r.b_row = g * p.N + r.n0;
+    r.out_row = (long long)(shared ? p.TK + j * p.T : eo[g]) + r.m0;
+    r.out_shared = false;
   } else {
-    A = a_routed + (size_t)(shared ? TK + j * T : expert_off[gr.g]) * KD;   // H buffer
-    O = shared ? out_shared + (size_t)j * T * N : out_routed + (size_t)expert_off[gr.g] * N;
-  }
-  const TE* B1 = wa + (size_t)gr.g * N * KD;
-  const TE* B3 = UP ? wb + (size_t)gr.g * N * KD : nullptr;
-  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-  float acc1[4][4] = {}, acc3[4][4] = {};
-  for (int k0 = 0; k0 < KD; k0 += kBK) {
-    for (int i = tid; i < kBM * kBK; i += 256) {
-      const int r = i / kBK, k = i % kBK;
-      const int gk = k0 + k;
-      const int ar = gr.m0 + r;
-      as[k][r] = (ar < gr.rows && gk < KD) ? Elem<TE>::to_f32(A[(size_t)ar * KD + gk]) : 0.0f;
-      const int bn = n0 + r;
-      b1s[k][r] = (bn < N && gk < KD) ? Elem<TE>::to_f32(B1[(size_t)bn * KD + gk]) : 0.0f;
-      if (UP) b3s[k][r] = (bn < N && gk < KD) ? Elem<TE>::to_f32(B3[(size_t)bn * KD + gk]) : 0.0f;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int k = 0; k < kBK; ++k) {
-      float a[4], b1[4], b3[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        a[i] = as[k][ty * 4 + i];
-        b1[i] = b1s[k][tx * 4 + i];
-        if (UP) b3[i] = b3s[k][tx * 4 + i];
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          acc1[i][q] = fmaf(a[i], b1[q], acc1[i][q]);
-          if (UP) acc3[i][q] = fmaf(a[i], b3[q], acc3[i][q]);
-        }
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = gr.m0 + ty * 4 + i;
-    if (r >= gr.rows) continue;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int n = n0 + tx * 4 + q;
-      if (n >= N) continue;
-      float v = acc1[i][q];
-      if (UP) v = (v / (1.0f + expf(-v))) * acc3[i][q];
-      O[(size_t)r * N + n] = Elem<TE>::from_f32(v);
-    }
+    r.n0 = n_tile * 256;
+    r.a_shared = false;
+    r.a_row = (shared ? p.TK + j * p.T : eo[g]) + r.m0;
+    r.b_row = g * p.N + r.n0;
+    r.out_row = (shared ? (long long)j * p.T : (long long)eo[g]) + r.m0;
+    r.out_shared = shared;
   }
 }
 
-template <typename TE>
+template <bool UP, bool F32>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmA_sh,
+                    const __grid_constant__ CUtensorMap tmB1,
+                    const __grid_constant__ CUtensorMap tmB3, const GemmArgs p) {
+  using TE = typename std::conditional<F32, float, __nv_bfloat16>::type;
+  constexpr int BK = F32 ? 32 : 64;           // elements per 128-byte row
+  constexpr int kMmaK = F32 ? 8 : 16;          // elements per MMA
+  constexpr int kMmaPerStage = BK / kMmaK;     // 4
+  constexpr uint32_t kIdesc = tc::instr_desc(F32, kBM, 256);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = base;
+  uint8_t* sB = base + kStages * kStageA;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * kStageB);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 1);
+  int* s_abort = reinterpret_cast<int*>(s_tmem + 1);
+  int32_t* s_ts = reinterpret_cast<int32_t*>(s_abort + 1);
+  int32_t* s_eo = s_ts + (p.G + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      tc::mbar_init(&tfull[a], 1);
+      tc::mbar_init(&tempty[a], 128);
+    }
+    tc::mbar_init(drain, 1);
+    *s_abort = 0;
+    tc::mbar_init_fence();
+    tc::tma_prefetch_map(&tmA);
+    tc::tma_prefetch_map(&tmA_sh);
+    tc::tma_prefetch_map(&tmB1);
+    tc::tma_prefetch_map(&tmB3);
+  }
+  for (int i = threadIdx.x; i <= p.G; i += kThreads) s_ts[i] = p.tile_start[i];
+  for (int i = threadIdx.x; i <= p.E; i += kThreads) s_eo[i] = p.expert_off[i];
+  if (warp == 2) {
+    tc::tmem_alloc(s_tmem, 2 * kAccCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *s_tmem;
+  const int total = s_ts[p.G] * p.NT;
+  const int nkb = (p.KD + BK - 1) / BK;
+  volatile int* abort = s_abort;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      Tile tl;
+      decode_tile<UP>(s_ts, s_eo, p, t, tl);
+      const CUtensorMap* amap = tl.a_shared ? &tmA_sh : &tmA;
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+        if (!tc::mbar_wait(&empty[s], ph ^ 1u, abort)) { ok = false; break; }
+        tc::mbar_expect_tx(&full[s], kStageA + kStageB);
+        tc::tma_load_2d(sA + s * kStageA, amap, &full[s], kb * BK, tl.a_row);
+        if (UP) {
+          tc::tma_load_2d(sB + s * kStageB, &tmB1, &full[s], kb * BK, tl.b_row);
+          tc::tma_load_2d(sB + s * kStageB + kStageB / 2, &tmB3, &full[s], kb * BK, tl.b_row);
+        } else {
+          tc::tma_load_2d(sB + s * kStageB, &tmB1, &full[s], kb * BK, tl.b_row);
+        }
+      }
+    }
+    if (!ok) {
+      *abort = 1;
+      record_error(p.st, kStatusTimeout, kTimeoutGemm, blockIdx.x);
+      // let the copies already issued land before the CTA's shared memory goes away
+      volatile int never = 0;
+      const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0;
+      for (uint32_t j = first; j < it; ++j)
+        tc::mbar_wait(&full[j % kStages], (j / kStages) & 1u, &never);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------------------- MMA issuer
+    uint32_t it = 0, tcount = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tcount) {
+      const uint32_t a = tcount & 1u, aph = (tcount >> 1) & 1u;
+      if (!tc::mbar_wait(&tempty[a], aph ^ 1u, abort)) { ok = false; break; }
+      tc::fence_after_sync();
+      const uint32_t d_tmem = tmem + a * kAccCols;
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+        if (!tc::mbar_wait(&full[s], ph, abort)) { ok = false; break; }
+        tc::fence_after_sync();
+        const uint64_t adesc = tc::sw128_kmajor_desc(tc::smem_u32(sA + s * kStageA));
+        const uint64_t bdesc = tc::sw128_kmajor_desc(tc::smem_u32(sB + s * kStageB));
+#pragma unroll
+        for (int k = 0; k < kMmaPerStage; ++k) {
+          const uint32_t acc = (kb > 0 || k > 0) ? 1u : 0u;
+          if (F32)
+            tc::mma_tf32(d_tmem, adesc + 2 * k, bdesc + 2 * k, kIdesc, acc);
+          else
+            tc::mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, kIdesc, acc);
+        }
+        tc::commit(&empty[s]);
+      }
+      if (!ok) break;
+      tc::commit(&tfull[a]);
+    }
+    if (!ok) {
+      *abort = 1;
+      record_error(p.st, kStatusTimeout, kTimeoutGemm, blockIdx.x);
+    }
+    // wait for every MMA this thread issued before TMEM is released
+    volatile int never = 0;
+    tc::commit(drain);
+    tc::mbar_wait(drain, 0, &never);
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    const int r = q * 32 + lane;  // accumulator row (TMEM lane) of this thread
+    uint32_t tcount = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++tcount) {
+      Tile tl;
+      decode_tile<UP>(s_ts, s_eo, p, t, tl);
+      const uint32_t a = tcount & 1u, aph = (tcount >> 1) & 1u;
+      if (!tc::mbar_wait(&tfull[a], aph, abort)) {
+        *abort = 1;
+        record_error(p.st, kStatusTimeout, kTimeoutGemm, blockIdx.x);
+        break;
+      }
+      tc::fence_after_sync();
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + a * kAccCols;
+      const bool row_ok = tl.m0 + r < tl.rows;
+      TE* out = static_cast<TE*>(tl.out_shared ? p.out_sh : p.out);
+      TE* orow = out + (size_t)(tl.out_row + r) * p.N;
+      constexpr int kVec = 16 / (int)sizeof(TE);
+      if (UP) {
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 32) {
+          uint32_t gv[32], uv[32];
+          tc::tmem_ld32(taddr + c, gv);
+          tc::tmem_ld32(taddr + 128 + c, uv);
+          tc::tmem_ld_wait();
+          float h[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float gg = __uint_as_float(gv[i]);
+            h[i] = gg / (1.0f + __expf(-gg)) * __uint_as_float(uv[i]);
+          }
+          if (row_ok) {
+#pragma unroll
+            for (int v = 0; v < 32 / kVec; ++v) {
+              const int n = tl.n0 + c + v * kVec;
+              if (n + kVec <= p.N)
+                *reinterpret_cast<uint4*>(orow + n) = pack16(h + v * kVec, (const TE*)nullptr);
+            }
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < 256; c += 32) {
+          uint32_t yv[32];
+          tc::tmem_ld32(taddr + c, yv);
+          tc::tmem_ld_wait();
+          float y[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) y[i] = __uint_as_float(yv[i]);
+          if (row_ok) {
+#pragma unroll
+            for (int v = 0; v < 32 / kVec; ++v) {
+              const int n = tl.n0 + c + v * kVec;
+              if (n + kVec <= p.N)
+                *reinterpret_cast<uint4*>(orow + n) = pack16(y + v * kVec, (const TE*)nullptr);
+            }
+          }
+        }
+      }
+      tc::fence_before_sync();
+      tc::mbar_arrive(&tempty[a]);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 2) tc::tmem_dealloc(tmem, 2 * kAccCols);
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 148;
+}
+
+template <bool UP, bool F32>
+cudaError_t launch_gemm(const CUtensorMap& A, const CUtensorMap& Ash, const CUtensorMap& B1,
+                        const CUtensorMap& B3, const GemmArgs& args, long long tile_bound,
+                        cudaStream_t s) {
+  auto kern = grouped_gemm_kernel<UP, F32>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int grid = (int)std::min<long long>(sm_count(), std::max<long long>(tile_bound, 1));
+  SMOE_COUNT_LAUNCH(1);
+  kern<<<grid, kThreads, kSmemBytes, s>>>(A, Ash, B1, B3, args);
+  return cudaGetLastError();
+}
+
+template <bool F32>
 cudaError_t run_ffn(const smoe_desc& d, const void* x_disp, const void* x,
                     const int32_t* expert_off, const void* w1, const void* w3, const void* w2,
                     void* y_disp, void* y_sh, void* ws, cudaStream_t s) {
   WsLayout L;
   ws_layout(d, &L);
   int32_t* tiles = ws_ptr<int32_t>(ws, L.tiles);
-  TE* hbuf = ws_ptr<TE>(ws, L.hbuf);
-  const int TK = d.T * d.K;
+  void* hbuf = ws_ptr<char>(ws, L.hbuf);
+  DeviceStatus* st = ws_ptr<DeviceStatus>(ws, L.status);
+  const int TK = d.T * d.K, G = d.E + d.n_shared;
+  const uint32_t box_k = F32 ? 32 : 64;
   SMOE_COUNT_LAUNCH(1);
-  tile_table_kernel<<<1, 32, 0, s>>>(expert_off, d.E, d.n_shared, d.T, TK, kBM, tiles,
-                                     ws_ptr<DeviceStatus>(ws, L.status));
-  const int max_tiles = ceil_div(TK, kBM) + d.E + d.n_shared * ceil_div(d.T, kBM);
-  dim3 g_up(max_tiles, ceil_div(d.F, kBN));
-  SMOE_COUNT_LAUNCH(1);
-  ffn_simt_kernel<TE, true><<<g_up, 256, 0, s>>>(
-      static_cast<const TE*>(x_disp), static_cast<const TE*>(x), expert_off, tiles,
-      static_cast<const TE*>(w1), static_cast<const TE*>(w3), hbuf, nullptr, d.E, d.n_shared,
-      d.T, TK, d.F, d.d);
-  dim3 g_dn(max_tiles, ceil_div(d.d, kBN));
-  SMOE_COUNT_LAUNCH(1);
-  ffn_simt_kernel<TE, false><<<g_dn, 256, 0, s>>>(
-      hbuf, nullptr, expert_off, tiles, static_cast<const TE*>(w2), nullptr,
-      static_cast<TE*>(y_disp), static_cast<TE*>(y_sh), d.E, d.n_shared, d.T, TK, d.d, d.F);
-  return cudaGetLastError();
+  tile_table_kernel<<<1, 32, 0, s>>>(expert_off, d.E, d.n_shared, d.T, TK, kBM, tiles, st);
+
+  const long long mtile_bound =
+      ceil_div(TK, kBM) + d.E + (long long)d.n_shared * ceil_div(d.T, kBM);
+  alignas(64) CUtensorMap tA, tAsh, tB1, tB3;
+  // up: A = x_disp [TK, d] (shared experts: x [T, d]); B = W1, W3 [(E+S) F, d]
+  if (!encode_tmap_2d(&tA, x_disp, F32, TK, d.d, kBM, box_k)) return cudaErrorInvalidValue;
+  if (!encode_tmap_2d(&tAsh, d.n_shared ? x : x_disp, F32, d.n_shared ? d.T : TK, d.d, kBM,
+                      box_k))
+    return cudaErrorInvalidValue;
+  if (!encode_tmap_2d(&tB1, w1, F32, (uint64_t)G * d.F, d.d, 128, box_k))
+    return cudaErrorInvalidValue;
+  if (!encode_tmap_2d(&tB3, w3, F32, (uint64_t)G * d.F, d.d, 128, box_k))
+    return cudaErrorInvalidValue;
+  GemmArgs up{expert_off, tiles, hbuf, nullptr, st, d.E, G, d.T, TK, d.F, d.d, ceil_div(d.F, 128)};
+  cudaError_t e = launch_gemm<true, F32>(tA, tAsh, tB1, tB3, up, mtile_bound * up.NT, s);
+  if (e != cudaSuccess) return e;
+
+  // down: A = H [TK + S T, F]; B = W2 [(E+S) d, F]
+  alignas(64) CUtensorMap dA, dB;
+  if (!encode_tmap_2d(&dA, hbuf, F32, (uint64_t)TK + (uint64_t)d.n_shared * d.T, d.F, kBM, box_k))
+    return cudaErrorInvalidValue;
+  if (!encode_tmap_2d(&dB, w2, F32, (uint64_t)G * d.d, d.F, 256, box_k))
+    return cudaErrorInvalidValue;
+  GemmArgs dn{expert_off, tiles, y_disp, y_sh, st, d.E, G, d.T, TK, d.d, d.F, ceil_div(d.d, 256)};
+  return launch_gemm<false, F32>(dA, dA, dB, dB, dn, mtile_bound * dn.NT, s);
+}
+
+// ------------------------------------------------------------------ tensor maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
 }
 
 }  // namespace
+
+bool encode_tmap_2d(CUtensorMap* map, const void* base, bool fp32, uint64_t rows, uint64_t cols,
+                    uint32_t box_rows, uint32_t box_cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) {
+    set_last_error(SMOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    return false;
+  }
+  const uint32_t esz = fp32 ? 4 : 2;
+  cuuint64_t dims[2] = {cols, rows > 0 ? rows : 1};
+  cuuint64_t strides[1] = {cols * esz};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                  2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_last_error(SMOE_ERR_CUDA, "cuTensorMapEncodeTiled rejected a tensor map");
+    return false;
+  }
+  return true;
+}
 
 cudaError_t launch_expert_ffn(const smoe_desc& d, const void* x_disp, const void* x,
                               const int32_t* expert_off, const void* w1, const void* w3,
                               const void* w2, void* y_disp, void* y_sh, void* ws,
                               cudaStream_t s) {
   if (d.dtype == SMOE_F32)
-    return run_ffn<float>(d, x_disp, x, expert_off, w1, w3, w2, y_disp, y_sh, ws, s);
-  return run_ffn<__nv_bfloat16>(d, x_disp, x, expert_off, w1, w3, w2, y_disp, y_sh, ws, s);
+    return run_ffn<true>(d, x_disp, x, expert_off, w1, w3, w2, y_disp, y_sh, ws, s);
+  return run_ffn<false>(d, x_disp, x, expert_off, w1, w3, w2, y_disp, y_sh, ws, s);
 }
 
 }  // namespace smoe
