@@ -39,7 +39,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--steps", type=int, default=100)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--impl", default="native", choices=["native", "reference"])
@@ -119,7 +119,7 @@ def ffn_flops(cfg) -> float:
 
 class ClockSampler:
     """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -133,7 +133,7 @@ class ClockSampler:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
             cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                   "-lms", "200"]
+                   "-lms", "50"]
             if self.gpu_id:
                 cmd += ["-i", self.gpu_id]
             self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"),
@@ -141,7 +141,9 @@ class ClockSampler:
         except (OSError, FileNotFoundError):
             self.proc = None
 
-    def stop(self) -> dict | None:
+    def stop(self, window=None) -> dict | None:
+        """Summarise the samples; with window = (t0, t1) in time.time() seconds keep only
+        the samples taken inside it (all samples if none fall inside)."""
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -156,6 +158,17 @@ class ClockSampler:
                 if len(parts) == 9:
                     rows.append(parts)
         os.unlink(self.path)
+        if window is not None:
+            import datetime
+            inside = []
+            for r in rows:
+                try:
+                    ts = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except ValueError:
+                    continue
+                if window[0] <= ts <= window[1]:
+                    inside.append(r)
+            rows = inside or rows
         if not rows:
             return None
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
@@ -200,13 +213,16 @@ class Workload:
             _, self.profile_idx, _ = O.route(px.float().cpu().numpy(),
                                              self.w_gate.float().cpu().numpy(), cfg.K, cfg.H)
         else:
-            pdesc = smoe.desc_from_config(cfg, T=n_prof)
+            chunk = min(n_prof, 8192)
+            pdesc = smoe.desc_from_config(cfg, T=chunk)
+            pws = smoe.workspace(pdesc, dev)
             pidx = torch.empty(n_prof, cfg.K, dtype=torch.int32, device=dev)
-            pw = torch.empty(n_prof, cfg.K, device=dev)
-            plog = torch.empty(n_prof, cfg.E, device=dev)
-            smoe.smoe_route(pdesc, px, self.w_gate, pidx, pw, logits_out=plog)
+            pw = torch.empty(chunk, cfg.K, device=dev)
+            for lo in range(0, n_prof, chunk):
+                smoe.smoe_route(pdesc, px[lo:lo + chunk], self.w_gate, pidx[lo:lo + chunk], pw,
+                                ws=pws)
             self.profile_idx = pidx.cpu().numpy()
-            del pw, plog
+            del pw, pws
         del px
         self.conf = profiling.confidence_table(
             pids, self.profile_idx, cfg.vocab, cfg.E, cfg.K,
@@ -351,7 +367,13 @@ def run_native(args):
     barrier(active)
     torch.cuda.synchronize()
     sampler.start()
+    t_s = time.perf_counter()
+    while time.perf_counter() - t_s < 0.4:   # keep the GPU busy while nvidia-smi starts
+        wl.step()
+        torch.cuda.synchronize()
+    barrier(active)
     launches0 = smoe.kernel_launches()
+    t_wall0 = time.time()
     wall0 = time.perf_counter()
     start.record()
     for i in range(args.steps):
@@ -359,8 +381,9 @@ def run_native(args):
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     launches = smoe.kernel_launches() - launches0
+    t_wall1 = time.time()
     barrier(active)
-    clocks = sampler.stop()
+    clocks = sampler.stop(window=(t_wall0, t_wall1))
     total_ms = start.elapsed_time(evs[-1][-1])
     stage_ms = {s: 0.0 for s in Workload.STAGES}
     for i in range(args.steps):

@@ -100,7 +100,8 @@ SMOE_API size_t smoe_workspace_size(const smoe_desc* desc);
  *                              logits: the lower expert index wins
  *   topk_w   [T, K] fp32       softmax over all E logits, taken at topk_idx
  *                              (divided by their sum when desc->renorm = 1)
- *   ws       workspace; holds the logits when logits_out is NULL                    */
+ *   ws       workspace (partial logits of the split gate GEMM); needed unless
+ *            logits_in is set                                                        */
 SMOE_API int smoe_route(const smoe_desc* desc, const void* x, const void* w_gate,
                         const float* logits_in, float* logits_out, int32_t* topk_idx,
                         float* topk_w, void* ws, size_t ws_bytes, void* stream);
@@ -139,7 +140,8 @@ SMOE_API int smoe_predict_shuffle(const smoe_desc* desc, const int32_t* token_id
  *     device current); make that first call before any stream capture begins.
  *   - All calls share the one array: calls that overlap on the GPU (different
  *     streams, or different host threads) race and must be serialised by the caller.
- *     Every call rewrites the parts it reads, so nothing carries over between calls.
+ *     Each call clears the histogram part of the array before using it and rewrites
+ *     the rest, so nothing carries over between calls.
  *   - Device data errors are not reported (there is no status word): an out-of-range
  *     token id or map entry gives partition 0, as in smoe_predict_shuffle.          */
 SMOE_API int smoe_predict_shuffle_noalloc(const smoe_desc* desc, const int32_t* token_ids,

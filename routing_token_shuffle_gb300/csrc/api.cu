@@ -148,6 +148,7 @@ bool ws_layout(const smoe_desc& d, WsLayout* L) {
   L->pf_qs = take(2 * T * dm * b);
   L->pf_logits = take(4 * 2 * T * E);
   L->pf_idx = take(4 * 2 * T * K);
+  L->route_part = take(4 * (size_t)route_splits(d, d.T) * T * E);
   L->total = off;
   return true;
 }
@@ -198,13 +199,10 @@ SMOE_API int smoe_route(const smoe_desc* desc, const void* x, const void* w_gate
     SMOE_PTR(w_gate);
   }
   if (desc->T == 0) return SMOE_OK;
-  if (!logits_in && !logits_out) SMOE_CHECK(check_ws(desc, ws, ws_bytes));
+  if (!logits_in) SMOE_CHECK(check_ws(desc, ws, ws_bytes));
   SMOE_CHECK(check_device());
-  WsLayout L;
-  ws_layout(*desc, &L);
-  float* lo = logits_out ? logits_out : (logits_in ? nullptr : ws_ptr<float>(ws, L.logits));
-  cudaError_t e = launch_route(*desc, desc->T, x, w_gate, logits_in, lo, topk_idx, topk_w,
-                               static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_route(*desc, desc->T, x, w_gate, logits_in, logits_out, topk_idx, topk_w,
+                               ws, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "route launch");
   return SMOE_OK;
 }
@@ -345,7 +343,7 @@ static int layer_forward_impl(const smoe_desc* d, const smoe_layer_weights* W,
   void* y_sh = d->n_shared ? ws_ptr<char>(ws, L.y_sh) : nullptr;
   (void)TK;
 
-  cudaError_t e = launch_route(*d, d->T, io->x, W->w_gate, nullptr, logits, idx, w, s);
+  cudaError_t e = launch_route(*d, d->T, io->x, W->w_gate, nullptr, logits, idx, w, ws, s);
   if (e != cudaSuccess) return cuda_fail(e, "route launch");
   e = launch_predict_shuffle(*d, io->token_ids, W->conf, W->expert_part, io->x, pred, perm,
                              part_off, io->skip_shuffle ? nullptr : x_shuf, ws, s);
@@ -464,10 +462,10 @@ SMOE_API int smoe_prefetch_predict(const smoe_desc* desc, const float* r, const 
   cudaError_t e = launch_prefetch_ln(*desc, r, d_l, y, gamma, beta, qs, s);
   if (e != cudaSuccess) return cuda_fail(e, "prefetch layernorm launch");
   e = launch_route(*desc, desc->T, qs, w_gate_next, nullptr, logits_q ? logits_q : lg, pred_idx,
-                   wq, s);
+                   wq, ws, s);
   if (e != cudaSuccess) return cuda_fail(e, "prefetch route launch");
   e = launch_route(*desc, desc->T, qs + T * desc->d * elem_size(*desc), w_gate_next, nullptr,
-                   logits_s ? logits_s : lg + T * desc->E, true_idx, wq + T * desc->K, s);
+                   logits_s ? logits_s : lg + T * desc->E, true_idx, wq + T * desc->K, ws, s);
   if (e != cudaSuccess) return cuda_fail(e, "prefetch route launch");
   e = launch_hits(*desc, pred_idx, true_idx, hits, s);
   if (e != cudaSuccess) return cuda_fail(e, "hits launch");

@@ -5,10 +5,18 @@
 // the router output of the full representation; the weights are the softmax over
 // all experts taken at the selected indices.
 //
+// bf16 layers: the gate GEMM runs on tcgen05 (M = 128 token rows, N = E rounded up to
+// 16, K split over KS CTAs so that even 32 row tiles fill the GPU); each split writes
+// fp32 partial logits, and the selection kernel adds the KS partials in split order.
+// fp32 layers keep an exact fp32-FMA gate GEMM: the tensor cores would round the
+// operands to tf32 and move logits by ~1e-3, enough to flip routing decisions.
+//
 // Selection: one warp per token, the token's fp32 logits spread over the lanes;
 // each pick is a butterfly argmax under the total order (logit descending, expert
 // index ascending), so equal logits (including +0 / -0) go to the lower index.
-#include "smoe_internal.cuh"
+#include <algorithm>
+
+#include "tc_common.cuh"
 
 namespace smoe {
 namespace {
@@ -17,19 +25,26 @@ constexpr int kSelWarps = 8;
 constexpr int kMaxPerLane = 16;  // E <= 512
 
 __global__ void __launch_bounds__(kSelWarps * 32)
-select_kernel(const float* __restrict__ logits, int T, int E, int K, int H, int renorm,
+select_kernel(const float* __restrict__ part, int KS, long long split_stride,
+              float* __restrict__ logits_out, int T, int E, int K, int H, int renorm,
               int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kSelWarps + (threadIdx.x >> 5);
   if (t >= T) return;
-  const float* row = logits + (size_t)t * E;
   float v[kMaxPerLane];
   float m = -INFINITY;
 #pragma unroll
   for (int i = 0; i < kMaxPerLane; ++i) {
     const int e = lane + 32 * i;
-    v[i] = e < E ? row[e] : -INFINITY;
-    m = fmaxf(m, v[i]);
+    float acc = -INFINITY;
+    if (e < E) {
+      const float* p = part + (size_t)t * E + e;
+      acc = p[0];
+      for (int s = 1; s < KS; ++s) acc += p[(size_t)s * split_stride];
+      if (logits_out) logits_out[(size_t)t * E + e] = acc;
+    }
+    v[i] = acc;
+    m = fmaxf(m, acc);
   }
 #pragma unroll
   for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
@@ -82,13 +97,13 @@ select_kernel(const float* __restrict__ logits, int T, int E, int K, int H, int 
   }
 }
 
+// ------------------------------------------------------------ fp32 gate GEMM
 // Tiled fp32-FMA gate GEMM: logits [rows, E] = x [rows, d] . w_gate[E, d]^T.
 constexpr int kBM = 64, kBN = 64, kBK = 32;
 
-template <typename TE>
 __global__ void __launch_bounds__(256)
-gate_gemm_kernel(const TE* __restrict__ x, const TE* __restrict__ wg, float* __restrict__ logits,
-                 int rows, int d, int E) {
+gate_gemm_f32_kernel(const float* __restrict__ x, const float* __restrict__ wg,
+                     float* __restrict__ logits, int rows, int d, int E) {
   __shared__ float xs[kBK][kBM + 4];
   __shared__ float gs[kBK][kBN + 4];
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
@@ -98,9 +113,9 @@ gate_gemm_kernel(const TE* __restrict__ x, const TE* __restrict__ wg, float* __r
     for (int i = tid; i < kBM * kBK; i += 256) {
       const int r = i / kBK, k = i % kBK;
       const int gr = m0 + r, gk = k0 + k;
-      xs[k][r] = (gr < rows && gk < d) ? Elem<TE>::to_f32(x[(size_t)gr * d + gk]) : 0.0f;
+      xs[k][r] = (gr < rows && gk < d) ? x[(size_t)gr * d + gk] : 0.0f;
       const int ge = n0 + r;
-      gs[k][r] = (ge < E && gk < d) ? Elem<TE>::to_f32(wg[(size_t)ge * d + gk]) : 0.0f;
+      gs[k][r] = (ge < E && gk < d) ? wg[(size_t)ge * d + gk] : 0.0f;
     }
     __syncthreads();
 #pragma unroll 8
@@ -127,32 +142,212 @@ gate_gemm_kernel(const TE* __restrict__ x, const TE* __restrict__ wg, float* __r
   }
 }
 
+// ------------------------------------------------------------ bf16 gate GEMM
+// One CTA per (128-row tile, K split). Warp 0: TMA producer (3-stage ring of
+// A 128 x 64 and B E_pad x 64 bf16 tiles, 128-byte swizzle); warp 1: tcgen05.mma
+// issuer (one N = E_pad MMA per 16-wide K step, two when E_pad > 256); warp 2: TMEM
+// allocation; warps 4-7: write the split's fp32 partial logits, one row per thread.
+constexpr int kGateStages = 3;
+constexpr uint32_t kGateA = 128 * 128;
+
+struct GateArgs {
+  float* part;              // [KS, rows, E]
+  DeviceStatus* st;
+  int rows, E, E_pad, nkb, KS;
+  uint32_t idesc1, idesc2;  // N = min(E_pad, 256) and E_pad - 256
+  uint32_t box_rows;        // B box rows (E_pad, or 256 when E_pad > 256)
+  uint32_t b_stage;         // bytes of one B stage
+  uint32_t tmem_cols;
+};
+
+__global__ void __launch_bounds__(256, 1)
+gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+               const GateArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = base;
+  uint8_t* sB = base + kGateStages * kGateA;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kGateStages * p.b_stage);
+  uint64_t* empty = full + kGateStages;
+  uint64_t* tfull = empty + kGateStages;
+  uint64_t* drain = tfull + 1;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 1);
+  int* s_abort = reinterpret_cast<int*>(s_tmem + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * 128, ks = blockIdx.y;
+  const int kb0 = (int)((long long)ks * p.nkb / p.KS);
+  const int kb1 = (int)((long long)(ks + 1) * p.nkb / p.KS);
+  const bool two = p.E_pad > 256;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kGateStages; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    tc::mbar_init(tfull, 1);
+    tc::mbar_init(drain, 1);
+    *s_abort = 0;
+    tc::mbar_init_fence();
+    tc::tma_prefetch_map(&tmX);
+    tc::tma_prefetch_map(&tmW);
+  }
+  if (warp == 2) {
+    tc::tmem_alloc(s_tmem, p.tmem_cols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *s_tmem;
+  volatile int* abort = s_abort;
+
+  if (warp == 0 && lane == 0) {
+    uint32_t it = 0;
+    bool ok = true;
+    const uint32_t tx = kGateA + (two ? 2u : 1u) * p.box_rows * 128u;
+    for (int kb = kb0; kb < kb1; ++kb, ++it) {
+      const uint32_t s = it % kGateStages, ph = (it / kGateStages) & 1u;
+      if (!tc::mbar_wait(&empty[s], ph ^ 1u, abort)) { ok = false; break; }
+      tc::mbar_expect_tx(&full[s], tx);
+      tc::tma_load_2d(sA + s * kGateA, &tmX, &full[s], kb * 64, m0);
+      tc::tma_load_2d(sB + s * p.b_stage, &tmW, &full[s], kb * 64, 0);
+      if (two) tc::tma_load_2d(sB + s * p.b_stage + 256 * 128, &tmW, &full[s], kb * 64, 256);
+    }
+    if (!ok) {
+      *abort = 1;
+      record_error(p.st, kStatusTimeout, kTimeoutGemm, blockIdx.x);
+      volatile int never = 0;
+      const uint32_t first = it > (uint32_t)kGateStages ? it - kGateStages : 0;
+      for (uint32_t j = first; j < it; ++j)
+        tc::mbar_wait(&full[j % kGateStages], (j / kGateStages) & 1u, &never);
+    }
+  } else if (warp == 1 && lane == 0) {
+    uint32_t it = 0;
+    bool ok = true;
+    for (int kb = kb0; kb < kb1; ++kb, ++it) {
+      const uint32_t s = it % kGateStages, ph = (it / kGateStages) & 1u;
+      if (!tc::mbar_wait(&full[s], ph, abort)) { ok = false; break; }
+      tc::fence_after_sync();
+      const uint64_t adesc = tc::sw128_kmajor_desc(tc::smem_u32(sA + s * kGateA));
+      const uint64_t bdesc = tc::sw128_kmajor_desc(tc::smem_u32(sB + s * p.b_stage));
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t acc = (kb > kb0 || k > 0) ? 1u : 0u;
+        tc::mma_bf16(tmem, adesc + 2 * k, bdesc + 2 * k, p.idesc1, acc);
+        if (two)
+          tc::mma_bf16(tmem + 256, adesc + 2 * k, bdesc + 2 * k + ((256 * 128) >> 4), p.idesc2,
+                       acc);
+      }
+      tc::commit(&empty[s]);
+    }
+    if (ok) {
+      tc::commit(tfull);
+    } else {
+      *abort = 1;
+      record_error(p.st, kStatusTimeout, kTimeoutGemm, blockIdx.x);
+    }
+    volatile int never = 0;
+    tc::commit(drain);
+    tc::mbar_wait(drain, 0, &never);
+  } else if (warp >= 4) {
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    if (tc::mbar_wait(tfull, 0, abort)) {
+      tc::fence_after_sync();
+      const int row = m0 + r;
+      float* out = p.part + ((size_t)ks * p.rows + row) * p.E;
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
+      const bool vec = (p.E & 3) == 0;
+      for (int c = 0; c < p.E_pad; c += 32) {
+        uint32_t v[32];
+        tc::tmem_ld32(taddr + c, v);
+        tc::tmem_ld_wait();
+        if (row < p.rows) {
+          if (vec && c + 32 <= p.E) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              *reinterpret_cast<uint4*>(out + c + 4 * i) =
+                  make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (c + i < p.E) out[c + i] = __uint_as_float(v[i]);
+          }
+        }
+      }
+    } else {
+      *abort = 1;
+      record_error(p.st, kStatusTimeout, kTimeoutGemm, blockIdx.x);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 2) tc::tmem_dealloc(tmem, p.tmem_cols);
+}
+
 }  // namespace
+
+int route_splits(const smoe_desc& d, int rows) {
+  if (d.dtype == SMOE_F32) return 1;
+  const int mt = ceil_div(rows, 128);
+  const int nkb = ceil_div(d.d, 64);
+  int ks = ceil_div(320, mt);
+  ks = std::min(ks, std::max(1, nkb / 2));
+  return std::max(1, std::min(ks, 16));
+}
 
 cudaError_t launch_route(const smoe_desc& d, int rows, const void* x, const void* w_gate,
                          const float* logits_in, float* logits_out, int32_t* topk_idx,
-                         float* topk_w, cudaStream_t s) {
-  const float* sel_in = logits_in;
-  if (!sel_in) {
-    dim3 grid(ceil_div(rows, kBM), ceil_div(d.E, kBN));
-    SMOE_COUNT_LAUNCH(1);
-    if (d.dtype == SMOE_F32)
-      gate_gemm_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(x),
-                                                   static_cast<const float*>(w_gate), logits_out,
-                                                   rows, d.d, d.E);
-    else
-      gate_gemm_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
-          static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w_gate),
-          logits_out, rows, d.d, d.E);
-    sel_in = logits_out;
-  } else if (logits_out && logits_out != logits_in) {
-    cudaError_t e = cudaMemcpyAsync(logits_out, logits_in, sizeof(float) * rows * d.E,
-                                    cudaMemcpyDeviceToDevice, s);
-    if (e != cudaSuccess) return e;
+                         float* topk_w, void* ws, cudaStream_t s) {
+  const float* part = logits_in;
+  int KS = 1;
+  if (!logits_in) {
+    WsLayout L;
+    ws_layout(d, &L);
+    float* pbuf = ws_ptr<float>(ws, L.route_part);
+    part = pbuf;
+    if (d.dtype == SMOE_F32) {
+      dim3 grid(ceil_div(rows, kBM), ceil_div(d.E, kBN));
+      SMOE_COUNT_LAUNCH(1);
+      gate_gemm_f32_kernel<<<grid, 256, 0, s>>>(static_cast<const float*>(x),
+                                                static_cast<const float*>(w_gate), pbuf, rows,
+                                                d.d, d.E);
+    } else {
+      KS = route_splits(d, rows);
+      const int E_pad = (d.E + 15) / 16 * 16;
+      GateArgs a;
+      a.part = pbuf;
+      a.st = ws_ptr<DeviceStatus>(ws, L.status);
+      a.rows = rows;
+      a.E = d.E;
+      a.E_pad = E_pad;
+      a.nkb = ceil_div(d.d, 64);
+      a.KS = KS;
+      a.idesc1 = tc::instr_desc(false, 128, std::min(E_pad, 256));
+      a.idesc2 = E_pad > 256 ? tc::instr_desc(false, 128, E_pad - 256) : 0u;
+      a.box_rows = E_pad > 256 ? 256u : (uint32_t)E_pad;
+      a.b_stage = E_pad > 256 ? 65536u : (uint32_t)E_pad * 128u;
+      a.tmem_cols = 32;
+      while (a.tmem_cols < (uint32_t)E_pad) a.tmem_cols <<= 1;
+      alignas(64) CUtensorMap tX, tW;
+      if (!encode_tmap_2d(&tX, x, false, rows, d.d, 128, 64)) return cudaErrorInvalidValue;
+      if (!encode_tmap_2d(&tW, w_gate, false, d.E, d.d, a.box_rows, 64))
+        return cudaErrorInvalidValue;
+      const size_t smem = 1024 + kGateStages * (kGateA + a.b_stage) + 128;
+      cudaError_t e = cudaFuncSetAttribute(gate_tc_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      dim3 grid(ceil_div(rows, 128), KS);
+      SMOE_COUNT_LAUNCH(1);
+      gate_tc_kernel<<<grid, 256, smem, s>>>(tX, tW, a);
+    }
   }
   SMOE_COUNT_LAUNCH(1);
-  select_kernel<<<ceil_div(rows, kSelWarps), kSelWarps * 32, 0, s>>>(sel_in, rows, d.E, d.K, d.H,
-                                                                    d.renorm, topk_idx, topk_w);
+  select_kernel<<<ceil_div(rows, kSelWarps), kSelWarps * 32, 0, s>>>(
+      part, KS, (long long)rows * d.E, logits_out == logits_in ? nullptr : logits_out, rows, d.E,
+      d.K, d.H, d.renorm, topk_idx, topk_w);
   return cudaGetLastError();
 }
 

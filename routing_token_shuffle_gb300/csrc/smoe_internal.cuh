@@ -88,6 +88,7 @@ struct WsLayout {
   size_t x_shuf, x_disp, hbuf, y_disp, y_sh;
   size_t x_dev, ids_dev, y_dev;     // staging for smoe_layer_forward_host
   size_t pf_qs, pf_logits, pf_idx;  // prefetch predictor: q and s rows, logits, routes
+  size_t route_part;                // gate GEMM partial logits [KS, T, E]
   size_t total;
 };
 
@@ -110,9 +111,11 @@ extern thread_local unsigned long long g_kernel_launches;
 
 // ---------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error; shapes are validated by the caller.
+int route_splits(const smoe_desc& d, int rows);  // K splits of the tensor-core gate GEMM
+
 cudaError_t launch_route(const smoe_desc& d, int rows, const void* x, const void* w_gate,
                          const float* logits_in, float* logits_out, int32_t* topk_idx,
-                         float* topk_w, cudaStream_t s);
+                         float* topk_w, void* ws, cudaStream_t s);
 
 cudaError_t launch_predict_shuffle(const smoe_desc& d, const int32_t* ids, const float* conf,
                                    const int32_t* emap, const void* x, int32_t* pred,

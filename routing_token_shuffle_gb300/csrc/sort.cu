@@ -28,78 +28,108 @@ __device__ __forceinline__ unsigned lanemask_lt() {
 }
 
 // ------------------------------------------------------------------ predict
-// One tile of kSortTile tokens per CTA, one warp per token: the warp stages the
-// token's C_p row in shared memory, lane p sums its partition's experts in
-// ascending e (one fp32 add each), and a butterfly argmax with the order
-// (score descending, partition ascending) picks pred[t]. Also counts the tile's
-// histogram of predicted partitions.
+// 64 tokens per CTA (a 1024-token sort tile spans 16 CTAs). The CTA stages the 64
+// C_p rows in shared memory in one burst, warp 0 lists each partition's experts in
+// ascending order (warp match), then one warp per token: lane p adds its partition's
+// row entries in that order (one fp32 add each, the oracle's order), and a butterfly
+// argmax with the order (score descending, partition ascending) picks pred[t]. The
+// CTA's partition counts are added to its sort tile's histogram entries (which the
+// launcher zeroes first).
+constexpr int kPredTokens = 64;
+
 __global__ void __launch_bounds__(kThreads)
 predict_hist_kernel(const int32_t* __restrict__ ids, const float* __restrict__ conf,
                     const int32_t* __restrict__ emap, int T, int E, int P, int vocab,
                     int32_t* __restrict__ pred, int32_t* __restrict__ hist, int ntiles,
                     DeviceStatus* st) {
+  extern __shared__ float s_rows[];          // [kPredTokens, E]
+  __shared__ int s_map[kMaxBuckets];
   __shared__ int s_list[kMaxBuckets];
   __shared__ int s_start[33];
+  __shared__ int s_fill[32];
   __shared__ int s_cnt[32];
-  __shared__ float s_row[kWarps][kMaxBuckets];
+  __shared__ int s_id[kPredTokens];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid < 32) s_cnt[tid] = 0;
+  const int t0 = blockIdx.x * kPredTokens;
+  const int n = min(kPredTokens, T - t0);
+  for (int e = tid; e < E; e += kThreads) {
+    const int p = emap[e];
+    const bool ok = (unsigned)p < (unsigned)P;
+    if (!ok && blockIdx.x == 0) record_error(st, kStatusData, kBadExpertPart, e);
+    s_map[e] = ok ? p : -1;
+  }
+  if (tid < 32) { s_cnt[tid] = 0; s_fill[tid] = 0; }
+  if (tid < n) {
+    const int id = ids[t0 + tid];
+    const bool ok = (unsigned)id < (unsigned)vocab;
+    if (!ok) record_error(st, kStatusData, kBadTokenId, t0 + tid);
+    s_id[tid] = ok ? id : -1;
+  }
+  __syncthreads();
+  for (int k = tid; k < n * E; k += kThreads) {
+    const int i = k / E, e = k - i * E;
+    const int id = s_id[i];
+    s_rows[k] = id >= 0 ? __ldg(conf + (size_t)id * E + e) : 0.0f;
+  }
   if (warp == 0) {
-    int c = 0;
-    for (int e = 0; e < E; ++e) c += (lane < P && emap[e] == lane);
-    int incl = c;
+    // partition p's experts in ascending order: s_list[s_start[p] .. s_start[p+1])
+    for (int c = 0; c < E; c += 32) {
+      const int e = c + lane;
+      const int p = e < E ? s_map[e] : -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, p);
+      if (p >= 0 && (peers & lanemask_lt()) == 0) s_fill[p] += __popc(peers);
+      __syncwarp();
+    }
+    const int cnt = lane < P ? s_fill[lane] : 0;
+    int incl = cnt;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       int y = __shfl_up_sync(0xffffffffu, incl, off);
       if (lane >= off) incl += y;
     }
-    int pos = incl - c;
-    if (lane < P) s_start[lane] = pos;
+    __syncwarp();
+    if (lane < P) { s_start[lane] = incl - cnt; s_fill[lane] = incl - cnt; }
     if (lane == P - 1) s_start[P] = incl;
-    for (int e = 0; e < E; ++e)
-      if (lane < P && emap[e] == lane) s_list[pos++] = e;
-    if (blockIdx.x == 0 && lane == 0)
-      for (int e = 0; e < E; ++e)
-        if (emap[e] < 0 || emap[e] >= P) record_error(st, kStatusData, kBadExpertPart, e);
+    __syncwarp();
+    for (int c = 0; c < E; c += 32) {
+      const int e = c + lane;
+      const int p = e < E ? s_map[e] : -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, p);
+      const int rank = __popc(peers & lanemask_lt());
+      if (p >= 0) s_list[s_fill[p] + rank] = e;
+      __syncwarp();
+      if (p >= 0 && rank == 0) s_fill[p] += __popc(peers);
+      __syncwarp();
+    }
   }
   __syncthreads();
-
-  const int t0 = blockIdx.x * kSortTile;
-  const int t1 = min(t0 + kSortTile, T);
-  for (int t = t0 + warp; t < t1; t += kWarps) {
-    const int id = ids[t];
-    int best = 0;
-    if ((unsigned)id < (unsigned)vocab) {
-      const float* row = conf + (size_t)id * E;
-      for (int e = lane; e < E; e += 32) s_row[warp][e] = __ldg(row + e);
-      __syncwarp();
-      float sc = -INFINITY;
-      if (lane < P) {
-        float acc = 0.0f;
-        for (int i = s_start[lane]; i < s_start[lane + 1]; ++i) acc = acc + s_row[warp][s_list[i]];
-        sc = acc;
-      }
-      int bi = lane;
-#pragma unroll
-      for (int off = 16; off; off >>= 1) {
-        const float os = __shfl_xor_sync(0xffffffffu, sc, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-        if (os > sc || (os == sc && oi < bi)) { sc = os; bi = oi; }
-      }
-      // only a NaN/inf row (outside the contract) can leave a lane >= P in front
-      best = (unsigned)bi < (unsigned)P ? bi : 0;
-      __syncwarp();
-    } else if (lane == 0) {
-      record_error(st, kStatusData, kBadTokenId, t);
+  for (int i = warp; i < n; i += kWarps) {
+    const float* row = s_rows + (size_t)i * E;
+    float sc = -INFINITY;
+    if (lane < P) {
+      float acc = 0.0f;
+      for (int j = s_start[lane]; j < s_start[lane + 1]; ++j) acc = acc + row[s_list[j]];
+      sc = acc;
     }
+    int bi = lane;
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+      const float os = __shfl_xor_sync(0xffffffffu, sc, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (os > sc || (os == sc && oi < bi)) { sc = os; bi = oi; }
+    }
+    // an invalid id, or a NaN/inf row (outside the contract), gives partition 0
+    const int best = (s_id[i] >= 0 && (unsigned)bi < (unsigned)P) ? bi : 0;
     if (lane == 0) {
-      pred[t] = best;
+      pred[t0 + i] = best;
       atomicAdd(&s_cnt[best], 1);
     }
   }
   __syncthreads();
-  if (tid < P) hist[tid * ntiles + blockIdx.x] = s_cnt[tid];
+  if (tid < P && s_cnt[tid] > 0) atomicAdd(&hist[tid * ntiles + t0 / kSortTile], s_cnt[tid]);
 }
+
+size_t predict_smem(int E) { return sizeof(float) * kPredTokens * E; }
 
 // ------------------------------------------------------------------ dispatch hist
 // Pairs q = s K + k in shuffled-slot order; bucket = expert idx[perm[s], k].
@@ -361,9 +391,14 @@ cudaError_t launch_predict_shuffle(const smoe_desc& d, const int32_t* ids, const
   int32_t* hist = ws_ptr<int32_t>(ws, L.sort_hist);
   int32_t* offs = ws_ptr<int32_t>(ws, L.sort_off);
   const int ntiles = ceil_div(d.T, kSortTile);
+  cudaError_t e = cudaMemsetAsync(hist, 0, sizeof(int32_t) * d.P * ntiles, s);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(predict_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)predict_smem(d.E));
+  if (e != cudaSuccess) return e;
   SMOE_COUNT_LAUNCH(1);
-  predict_hist_kernel<<<ntiles, kThreads, 0, s>>>(ids, conf, emap, d.T, d.E, d.P, d.vocab, pred,
-                                                  hist, ntiles, st);
+  predict_hist_kernel<<<ceil_div(d.T, kPredTokens), kThreads, predict_smem(d.E), s>>>(
+      ids, conf, emap, d.T, d.E, d.P, d.vocab, pred, hist, ntiles, st);
   SMOE_COUNT_LAUNCH(1);
   scan_kernel<<<1, 1024, 0, s>>>(hist, offs, d.P * ntiles, d.P, ntiles, d.T, part_off);
   SMOE_COUNT_LAUNCH(1);
@@ -496,16 +531,21 @@ extern "C" SMOE_API int smoe_predict_shuffle_noalloc(const smoe_desc* desc,
     cudaError_t e = cudaMemsetAsync(part_off, 0, sizeof(int32_t) * (desc->P + 1), s);
     return e == cudaSuccess ? SMOE_OK : set_last_error(SMOE_ERR_CUDA, cudaGetErrorString(e));
   }
-  // Both halves of the scratch are fully written before they are read (every tile
-  // writes its P histogram entries; the scan writes every offset), so nothing needs
-  // clearing between calls. Device data errors are not reported by this variant:
-  // an out-of-range id is treated as partition 0, as in smoe_predict_shuffle.
+  // The histogram part of the scratch is cleared at the start of every call (the
+  // predict kernel adds into it); the offsets part is fully rewritten by the scan.
+  // Device data errors are not reported by this variant: an out-of-range id is
+  // treated as partition 0, as in smoe_predict_shuffle.
   int32_t* hist = scratch;
   int32_t* offs = scratch + 32 * kNoAllocMaxTiles;
   const smoe_desc& d = *desc;
+  cudaError_t ce = cudaMemsetAsync(hist, 0, sizeof(int32_t) * d.P * ntiles, s);
+  if (ce == cudaSuccess)
+    ce = cudaFuncSetAttribute(predict_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)predict_smem(d.E));
+  if (ce != cudaSuccess) return set_last_error(SMOE_ERR_CUDA, cudaGetErrorString(ce));
   SMOE_COUNT_LAUNCH(1);
-  predict_hist_kernel<<<ntiles, kThreads, 0, s>>>(token_ids, conf, expert_part, d.T, d.E, d.P,
-                                                  d.vocab, pred_part, hist, ntiles, nullptr);
+  predict_hist_kernel<<<ceil_div(d.T, kPredTokens), kThreads, predict_smem(d.E), s>>>(
+      token_ids, conf, expert_part, d.T, d.E, d.P, d.vocab, pred_part, hist, ntiles, nullptr);
   SMOE_COUNT_LAUNCH(1);
   scan_kernel<<<1, 1024, 0, s>>>(hist, offs, d.P * ntiles, d.P, ntiles, d.T, part_off);
   SMOE_COUNT_LAUNCH(1);
