@@ -10,67 +10,108 @@ namespace smoe {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kMaxPer = 32;  // d <= 8192
+constexpr int kMaxChunks = 8;  // 4-element chunks per thread: d <= 8192
 
-__device__ __forceinline__ float block_sum(float v, float* red) {
+__device__ __forceinline__ float2 block_sum2(float2 v, float2* red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
-  for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  for (int off = 16; off; off >>= 1) {
+    v.x += __shfl_xor_sync(0xffffffffu, v.x, off);
+    v.y += __shfl_xor_sync(0xffffffffu, v.y, off);
+  }
   __syncthreads();
   if (lane == 0) red[warp] = v;
   __syncthreads();
-  float s = 0.0f;
+  float2 s = make_float2(0.0f, 0.0f);
 #pragma unroll
-  for (int w = 0; w < kThreads / 32; ++w) s += red[w];
+  for (int w = 0; w < kThreads / 32; ++w) {
+    s.x += red[w].x;
+    s.y += red[w].y;
+  }
   return s;
 }
 
+__device__ __forceinline__ void load4(const float* p, float* v) {
+  const float4 u = *reinterpret_cast<const float4*>(p);
+  v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+}
+__device__ __forceinline__ void load4(const __nv_bfloat16* p, float* v) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  v[0] = __uint_as_float(u.x << 16); v[1] = __uint_as_float(u.x & 0xffff0000u);
+  v[2] = __uint_as_float(u.y << 16); v[3] = __uint_as_float(u.y & 0xffff0000u);
+}
+__device__ __forceinline__ void store4(float* p, const float* v) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+}
+__device__ __forceinline__ void store4(__nv_bfloat16* p, const float* v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]);
+  *reinterpret_cast<uint2*>(p) =
+      make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+}
+
 // Row t: q = LN(d_l + r_t) -> qs[t], s = LN(r_t + y_t) -> qs[T + t]; biased variance,
-// eps 1e-5, two passes over values held in registers, output rounded to TE.
+// eps 1e-5, two passes over values held in registers (4-element chunks), output
+// rounded to TE.
 template <typename TE>
 __global__ void __launch_bounds__(kThreads)
 ln_pair_kernel(const float* __restrict__ r, const float* __restrict__ d_l,
                const TE* __restrict__ y, const float* __restrict__ gamma,
                const float* __restrict__ beta, TE* __restrict__ qs, int T, int d) {
-  __shared__ float red[kThreads / 32];
+  __shared__ float2 red[kThreads / 32];
   const int t = blockIdx.x;
   const float* rr = r + (size_t)t * d;
   const TE* yy = y + (size_t)t * d;
-  float a[kMaxPer], b[kMaxPer];
-  float sa = 0.0f, sb = 0.0f;
+  float a[kMaxChunks][4], b[kMaxChunks][4];
+  float2 sum = make_float2(0.0f, 0.0f);
 #pragma unroll
-  for (int i = 0; i < kMaxPer; ++i) {
-    const int j = threadIdx.x + i * kThreads;
-    a[i] = b[i] = 0.0f;
+  for (int i = 0; i < kMaxChunks; ++i) {
+    const int j = 4 * (threadIdx.x + i * kThreads);
     if (j < d) {
-      const float rv = rr[j];
-      a[i] = d_l[j] + rv;
-      b[i] = rv + Elem<TE>::to_f32(yy[j]);
-      sa += a[i];
-      sb += b[i];
+      float rv[4], dv[4], yv[4];
+      load4(rr + j, rv);
+      load4(d_l + j, dv);
+      load4(yy + j, yv);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        a[i][c] = dv[c] + rv[c];
+        b[i][c] = rv[c] + yv[c];
+        sum.x += a[i][c];
+        sum.y += b[i][c];
+      }
     }
   }
-  const float ma = block_sum(sa, red) / d;
-  const float mb = block_sum(sb, red) / d;
-  float va = 0.0f, vb = 0.0f;
+  const float2 tot = block_sum2(sum, red);
+  const float ma = tot.x / d, mb = tot.y / d;
+  float2 sq = make_float2(0.0f, 0.0f);
 #pragma unroll
-  for (int i = 0; i < kMaxPer; ++i) {
-    const int j = threadIdx.x + i * kThreads;
+  for (int i = 0; i < kMaxChunks; ++i) {
+    const int j = 4 * (threadIdx.x + i * kThreads);
     if (j < d) {
-      va += (a[i] - ma) * (a[i] - ma);
-      vb += (b[i] - mb) * (b[i] - mb);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        sq.x += (a[i][c] - ma) * (a[i][c] - ma);
+        sq.y += (b[i][c] - mb) * (b[i][c] - mb);
+      }
     }
   }
-  const float ia = rsqrtf(block_sum(va, red) / d + 1e-5f);
-  const float ib = rsqrtf(block_sum(vb, red) / d + 1e-5f);
+  const float2 var = block_sum2(sq, red);
+  const float ia = rsqrtf(var.x / d + 1e-5f), ib = rsqrtf(var.y / d + 1e-5f);
   TE* q = qs + (size_t)t * d;
   TE* s = qs + ((size_t)T + t) * d;
 #pragma unroll
-  for (int i = 0; i < kMaxPer; ++i) {
-    const int j = threadIdx.x + i * kThreads;
+  for (int i = 0; i < kMaxChunks; ++i) {
+    const int j = 4 * (threadIdx.x + i * kThreads);
     if (j < d) {
-      q[j] = Elem<TE>::from_f32((a[i] - ma) * ia * gamma[j] + beta[j]);
-      s[j] = Elem<TE>::from_f32((b[i] - mb) * ib * gamma[j] + beta[j]);
+      float g[4], bt[4], oq[4], os[4];
+      load4(gamma + j, g);
+      load4(beta + j, bt);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        oq[c] = (a[i][c] - ma) * ia * g[c] + bt[c];
+        os[c] = (b[i][c] - mb) * ib * g[c] + bt[c];
+      }
+      store4(q + j, oq);
+      store4(s + j, os);
     }
   }
 }

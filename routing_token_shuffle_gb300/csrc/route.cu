@@ -22,8 +22,9 @@ namespace smoe {
 namespace {
 
 constexpr int kSelWarps = 8;
-constexpr int kMaxPerLane = 16;  // E <= 512
 
+// kMaxPerLane logits per lane: E <= 32 * kMaxPerLane (4, 8 or 16).
+template <int kMaxPerLane>
 __global__ void __launch_bounds__(kSelWarps * 32)
 select_kernel(const float* __restrict__ part, int KS, long long split_stride,
               float* __restrict__ logits_out, int T, int E, int K, int H, int renorm,
@@ -293,7 +294,7 @@ int route_splits(const smoe_desc& d, int rows) {
   if (d.dtype == SMOE_F32) return 1;
   const int mt = ceil_div(rows, 128);
   const int nkb = ceil_div(d.d, 64);
-  int ks = ceil_div(320, mt);
+  int ks = ceil_div(160, mt);   // enough (row tile, split) CTAs to cover the SMs once
   ks = std::min(ks, std::max(1, nkb / 2));
   return std::max(1, std::min(ks, 16));
 }
@@ -344,10 +345,19 @@ cudaError_t launch_route(const smoe_desc& d, int rows, const void* x, const void
       gate_tc_kernel<<<grid, 256, smem, s>>>(tX, tW, a);
     }
   }
+  float* lo = logits_out == logits_in ? nullptr : logits_out;
+  const long long stride = (long long)rows * d.E;
+  const dim3 grid(ceil_div(rows, kSelWarps)), block(kSelWarps * 32);
   SMOE_COUNT_LAUNCH(1);
-  select_kernel<<<ceil_div(rows, kSelWarps), kSelWarps * 32, 0, s>>>(
-      part, KS, (long long)rows * d.E, logits_out == logits_in ? nullptr : logits_out, rows, d.E,
-      d.K, d.H, d.renorm, topk_idx, topk_w);
+  if (d.E <= 128)
+    select_kernel<4><<<grid, block, 0, s>>>(part, KS, stride, lo, rows, d.E, d.K, d.H, d.renorm,
+                                            topk_idx, topk_w);
+  else if (d.E <= 256)
+    select_kernel<8><<<grid, block, 0, s>>>(part, KS, stride, lo, rows, d.E, d.K, d.H, d.renorm,
+                                            topk_idx, topk_w);
+  else
+    select_kernel<16><<<grid, block, 0, s>>>(part, KS, stride, lo, rows, d.E, d.K, d.H, d.renorm,
+                                             topk_idx, topk_w);
   return cudaGetLastError();
 }
 
