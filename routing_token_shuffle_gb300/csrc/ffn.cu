@@ -326,6 +326,242 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   if (warp == 2) tc::tmem_dealloc(tmem, 2 * kAccCols);
 }
 
+// ------------------------------------------------------------------ two-SM variant
+// A cluster of two CTAs (on the two SMs of a TPC) computes 256 x 256 tiles with
+// tcgen05.mma.cta_group::2: each CTA loads its own 128 rows of A and 128 rows of B
+// (up: the leader W1, the peer W3; down: each half of the 256 W2 rows), so each SM
+// receives 32 KB per 64-wide k-block instead of 48 KB for the same MMA rate. The
+// leader's thread issues the MMAs; stage bytes of both CTAs complete on the leader's
+// `full` barrier; MMA completion is multicast to both CTAs' `empty` and `tfull`; both
+// epilogues drain their own 128 TMEM lanes and arrive on the leader's `tempty`.
+constexpr int kPairStages = 6;
+constexpr uint32_t kPairStage = 128 * 128;  // A half or B half: 128 rows x 128 bytes
+constexpr size_t kPairSmemBytes =
+    1024 + kPairStages * 2 * kPairStage + 256 + 4 * (kMaxGroups + 1 + 513 + 4);
+
+template <bool UP>
+__device__ __forceinline__ void decode_pair_tile(const int32_t* ts, const int32_t* eo,
+                                                 const GemmArgs& p, int t, uint32_t rank,
+                                                 Tile& r) {
+  int lo = 0, hi = p.G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (ts[mid] * p.NT <= t) lo = mid; else hi = mid - 1;
+  }
+  const int g = lo;
+  const int mt = ts[g + 1] - ts[g];  // 256-row pairs of this group
+  const int local = t - ts[g] * p.NT;
+  const int n_tile = local / mt, m_pair = local - n_tile * mt;
+  r.g = g;
+  r.m0 = m_pair * 256 + (int)rank * 128;
+  const bool shared = g >= p.E;
+  const int j = g - p.E;
+  r.rows = shared ? p.T : eo[g + 1] - eo[g];
+  if (UP) {
+    r.n0 = n_tile * 128;
+    r.a_shared = shared;
+    r.a_row = (shared ? 0 : eo[g]) + r.m0;
+    r.b_row = g * p.N + r.n0;  // leader: W1 rows, peer: W3 rows
+    r.out_row = (long long)(shared ? p.TK + j * p.T : eo[g]) + r.m0;
+    r.out_shared = false;
+  } else {
+    r.n0 = n_tile * 256;
+    r.a_shared = false;
+    r.a_row = (shared ? p.TK + j * p.T : eo[g]) + r.m0;
+    r.b_row = g * p.N + r.n0 + (int)rank * 128;
+    r.out_row = (shared ? (long long)j * p.T : (long long)eo[g]) + r.m0;
+    r.out_shared = shared;
+  }
+}
+
+template <bool UP>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                         const __grid_constant__ CUtensorMap tmA_sh,
+                         const __grid_constant__ CUtensorMap tmB1,
+                         const __grid_constant__ CUtensorMap tmB3, const GemmArgs p) {
+  using TE = __nv_bfloat16;
+  constexpr uint32_t kIdesc = tc::instr_desc(false, 256, 256);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = base;
+  uint8_t* sB = base + kPairStages * kPairStage;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kPairStages * kPairStage);
+  uint64_t* empty = full + kPairStages;
+  uint64_t* tfull = empty + kPairStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 1);
+  int* s_abort = reinterpret_cast<int*>(s_tmem + 1);
+  int32_t* s_ts = reinterpret_cast<int32_t*>(s_abort + 1);
+  int32_t* s_eo = s_ts + (p.G + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = tc::cluster_rank();
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      tc::mbar_init(&tfull[a], 1);
+      tc::mbar_init(&tempty[a], 256);
+    }
+    tc::mbar_init(drain, 1);
+    *s_abort = 0;
+    tc::mbar_init_fence();
+    tc::tma_prefetch_map(&tmA);
+    tc::tma_prefetch_map(&tmA_sh);
+    tc::tma_prefetch_map(&tmB1);
+    tc::tma_prefetch_map(&tmB3);
+  }
+  for (int i = threadIdx.x; i <= p.G; i += kThreads) s_ts[i] = p.tile_start[i];
+  for (int i = threadIdx.x; i <= p.E; i += kThreads) s_eo[i] = p.expert_off[i];
+  if (warp == 2) {
+    tc::tmem_alloc_pair(s_tmem, 2 * kAccCols);
+    tc::tmem_relinquish_pair();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::cluster_sync();  // both CTAs' barriers are initialised before any remote signal
+  tc::fence_after_sync();
+  const uint32_t tmem = *s_tmem;
+  const int total = s_ts[p.G] * p.NT;
+  const int nkb = (p.KD + 63) / 64;
+  volatile int* abort = s_abort;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    const CUtensorMap* bmap = (UP && rank == 1) ? &tmB3 : &tmB1;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = pair; t < total && ok; t += npairs) {
+      Tile tl;
+      decode_pair_tile<UP>(s_ts, s_eo, p, t, rank, tl);
+      const CUtensorMap* amap = tl.a_shared ? &tmA_sh : &tmA;
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const uint32_t s = it % kPairStages, ph = (it / kPairStages) & 1u;
+        if (!tc::mbar_wait(&empty[s], ph ^ 1u, abort)) { ok = false; break; }
+        const uint32_t leader_full = tc::cluster_addr(&full[s], 0);
+        if (rank == 0) tc::mbar_expect_tx(&full[s], 4 * kPairStage);
+        tc::tma_load_2d_pair(sA + s * kPairStage, amap, leader_full, kb * 64, tl.a_row);
+        tc::tma_load_2d_pair(sB + s * kPairStage, bmap, leader_full, kb * 64, tl.b_row);
+      }
+    }
+    if (!ok) {
+      *abort = 1;
+      record_error(p.st, kStatusTimeout, kTimeoutGemm, blockIdx.x);
+    }
+  } else if (warp == 1 && lane == 0 && rank == 0) {
+    // ---------------------------------------------------------------- MMA issuer (leader)
+    uint32_t it = 0, tcount = 0;
+    bool ok = true;
+    for (int t = pair; t < total && ok; t += npairs, ++tcount) {
+      const uint32_t a = tcount & 1u, aph = (tcount >> 1) & 1u;
+      if (!tc::mbar_wait(&tempty[a], aph ^ 1u, abort)) { ok = false; break; }
+      tc::fence_after_sync();
+      const uint32_t d_tmem = tmem + a * kAccCols;
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const uint32_t s = it % kPairStages, ph = (it / kPairStages) & 1u;
+        if (!tc::mbar_wait(&full[s], ph, abort)) { ok = false; break; }
+        tc::fence_after_sync();
+        const uint64_t adesc = tc::sw128_kmajor_desc(tc::smem_u32(sA + s * kPairStage));
+        const uint64_t bdesc = tc::sw128_kmajor_desc(tc::smem_u32(sB + s * kPairStage));
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          tc::mma_bf16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, kIdesc,
+                            (kb > 0 || k > 0) ? 1u : 0u);
+        tc::commit_pair(&empty[s], 0x3);
+      }
+      if (!ok) break;
+      tc::commit_pair(&tfull[a], 0x3);
+    }
+    if (!ok) {
+      *abort = 1;
+      record_error(p.st, kStatusTimeout, kTimeoutGemm, blockIdx.x);
+    }
+    volatile int never = 0;
+    tc::commit_pair(drain, 0x1);
+    tc::mbar_wait(drain, 0, &never);
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- epilogue (both CTAs)
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    uint32_t tcount = 0;
+    for (int t = pair; t < total; t += npairs, ++tcount) {
+      Tile tl;
+      decode_pair_tile<UP>(s_ts, s_eo, p, t, rank, tl);
+      const uint32_t a = tcount & 1u, aph = (tcount >> 1) & 1u;
+      if (!tc::mbar_wait(&tfull[a], aph, abort)) {
+        *abort = 1;
+        record_error(p.st, kStatusTimeout, kTimeoutGemm, blockIdx.x);
+        break;
+      }
+      tc::fence_after_sync();
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + a * kAccCols;
+      const bool row_ok = tl.m0 + r < tl.rows;
+      TE* out = static_cast<TE*>(tl.out_shared ? p.out_sh : p.out);
+      TE* orow = out + (size_t)(tl.out_row + r) * p.N;
+      if (UP) {
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 32) {
+          uint32_t gv[32], uv[32];
+          tc::tmem_ld32(taddr + c, gv);
+          tc::tmem_ld32(taddr + 128 + c, uv);
+          tc::tmem_ld_wait();
+          float h[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float gg = __uint_as_float(gv[i]);
+            h[i] = gg / (1.0f + __expf(-gg)) * __uint_as_float(uv[i]);
+          }
+          if (row_ok) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const int n = tl.n0 + c + v * 8;
+              if (n + 8 <= p.N)
+                *reinterpret_cast<uint4*>(orow + n) = pack16(h + v * 8, (const TE*)nullptr);
+            }
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < 256; c += 32) {
+          uint32_t yv[32];
+          tc::tmem_ld32(taddr + c, yv);
+          tc::tmem_ld_wait();
+          float y[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) y[i] = __uint_as_float(yv[i]);
+          if (row_ok) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const int n = tl.n0 + c + v * 8;
+              if (n + 8 <= p.N)
+                *reinterpret_cast<uint4*>(orow + n) = pack16(y + v * 8, (const TE*)nullptr);
+            }
+          }
+        }
+      }
+      tc::fence_before_sync();
+      tc::mbar_arrive_cluster(tc::cluster_addr(&tempty[a], 0));
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::cluster_sync();
+  tc::fence_after_sync();
+  if (warp == 2) tc::tmem_dealloc_pair(tmem, 2 * kAccCols);
+}
+
+template <bool UP>
+cudaError_t launch_gemm_pair(const CUtensorMap& A, const CUtensorMap& Ash, const CUtensorMap& B1,
+                             const CUtensorMap& B3, const GemmArgs& args, long long tile_bound,
+                             cudaStream_t s);
+
 int sm_count() {
   int dev = 0, n = 0;
   cudaGetDevice(&dev);
@@ -347,6 +583,37 @@ cudaError_t launch_gemm(const CUtensorMap& A, const CUtensorMap& Ash, const CUte
   return cudaGetLastError();
 }
 
+template <bool UP>
+cudaError_t launch_gemm_pair(const CUtensorMap& A, const CUtensorMap& Ash, const CUtensorMap& B1,
+                             const CUtensorMap& B3, const GemmArgs& args, long long tile_bound,
+                             cudaStream_t s) {
+  auto kern = grouped_gemm_pair_kernel<UP>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kPairSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int pairs = (int)std::min<long long>(sm_count() / 2, std::max<long long>(tile_bound, 1));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kPairSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  SMOE_COUNT_LAUNCH(1);
+  return cudaLaunchKernelEx(&cfg, kern, A, Ash, B1, B3, args);
+}
+
+// Two-SM tiles pay off when experts hold enough rows that a 256-row tile is rarely
+// mostly padding.
+bool use_pair_tiles(const smoe_desc& d) {
+  return d.dtype == SMOE_BF16 && (long long)d.T * d.K >= 512LL * d.E;
+}
+
 template <bool F32>
 cudaError_t run_ffn(const smoe_desc& d, const void* x_disp, const void* x,
                     const int32_t* expert_off, const void* w1, const void* w3, const void* w2,
@@ -358,11 +625,13 @@ cudaError_t run_ffn(const smoe_desc& d, const void* x_disp, const void* x,
   DeviceStatus* st = ws_ptr<DeviceStatus>(ws, L.status);
   const int TK = d.T * d.K, G = d.E + d.n_shared;
   const uint32_t box_k = F32 ? 32 : 64;
+  const bool pairs = !F32 && use_pair_tiles(d);
+  const int bm = pairs ? 256 : kBM;
   SMOE_COUNT_LAUNCH(1);
-  tile_table_kernel<<<1, 32, 0, s>>>(expert_off, d.E, d.n_shared, d.T, TK, kBM, tiles, st);
+  tile_table_kernel<<<1, 32, 0, s>>>(expert_off, d.E, d.n_shared, d.T, TK, bm, tiles, st);
 
   const long long mtile_bound =
-      ceil_div(TK, kBM) + d.E + (long long)d.n_shared * ceil_div(d.T, kBM);
+      ceil_div(TK, bm) + d.E + (long long)d.n_shared * ceil_div(d.T, bm);
   alignas(64) CUtensorMap tA, tAsh, tB1, tB3;
   // up: A = x_disp [TK, d] (shared experts: x [T, d]); B = W1, W3 [(E+S) F, d]
   if (!encode_tmap_2d(&tA, x_disp, F32, TK, d.d, kBM, box_k)) return cudaErrorInvalidValue;
@@ -374,17 +643,19 @@ cudaError_t run_ffn(const smoe_desc& d, const void* x_disp, const void* x,
   if (!encode_tmap_2d(&tB3, w3, F32, (uint64_t)G * d.F, d.d, 128, box_k))
     return cudaErrorInvalidValue;
   GemmArgs up{expert_off, tiles, hbuf, nullptr, st, d.E, G, d.T, TK, d.F, d.d, ceil_div(d.F, 128)};
-  cudaError_t e = launch_gemm<true, F32>(tA, tAsh, tB1, tB3, up, mtile_bound * up.NT, s);
+  cudaError_t e = pairs ? launch_gemm_pair<true>(tA, tAsh, tB1, tB3, up, mtile_bound * up.NT, s)
+                        : launch_gemm<true, F32>(tA, tAsh, tB1, tB3, up, mtile_bound * up.NT, s);
   if (e != cudaSuccess) return e;
 
   // down: A = H [TK + S T, F]; B = W2 [(E+S) d, F]
   alignas(64) CUtensorMap dA, dB;
   if (!encode_tmap_2d(&dA, hbuf, F32, (uint64_t)TK + (uint64_t)d.n_shared * d.T, d.F, kBM, box_k))
     return cudaErrorInvalidValue;
-  if (!encode_tmap_2d(&dB, w2, F32, (uint64_t)G * d.d, d.F, 256, box_k))
+  if (!encode_tmap_2d(&dB, w2, F32, (uint64_t)G * d.d, d.F, pairs ? 128 : 256, box_k))
     return cudaErrorInvalidValue;
   GemmArgs dn{expert_off, tiles, y_disp, y_sh, st, d.E, G, d.T, TK, d.d, d.F, ceil_div(d.d, 256)};
-  return launch_gemm<false, F32>(dA, dA, dB, dB, dn, mtile_bound * dn.NT, s);
+  return pairs ? launch_gemm_pair<false>(dA, dA, dB, dB, dn, mtile_bound * dn.NT, s)
+               : launch_gemm<false, F32>(dA, dA, dB, dB, dn, mtile_bound * dn.NT, s);
 }
 
 // ------------------------------------------------------------------ tensor maps

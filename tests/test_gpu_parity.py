@@ -395,3 +395,39 @@ def test_empty_batch():
     torch.cuda.synchronize()
     assert to_np(off).tolist() == [0, 0, 0]
     del e
+
+
+@pytest.mark.parametrize("T,E,K,S,d,F", [(2500, 8, 2, 0, 256, 384), (1537, 4, 2, 1, 512, 256),
+                                         (4099, 16, 2, 0, 128, 640)])
+def test_expert_ffn_two_sm_tiles_ragged(T, E, K, S, d, F):
+    """Shapes with at least 512 rows per expert take the two-SM (256-row) tiles; ragged
+    expert segments, a partial last n-tile (F = 640, 384) and a shared expert."""
+    assert T * K >= 512 * E
+    g = torch.Generator(device="cuda").manual_seed(T + E)
+    x = (torch.randn(T, d, generator=g, device="cuda")).to(torch.bfloat16)
+    w1 = (torch.randn(E + S, F, d, generator=g, device="cuda") / d ** 0.5).to(torch.bfloat16)
+    w3 = (torch.randn(E + S, F, d, generator=g, device="cuda") / d ** 0.5).to(torch.bfloat16)
+    w2 = (torch.randn(E + S, d, F, generator=g, device="cuda") / F ** 0.5).to(torch.bfloat16)
+    logits = torch.randn(T, E, generator=g, device="cuda") * 2
+    desc = smoe.make_desc(T, d, E, K, 1, F, S, 2, 100, "bf16")
+    ws = smoe.workspace(desc)
+    idx, w = i32(T, K), f32(T, K)
+    smoe.smoe_route(desc, None, None, idx, w, logits_in=logits, ws=ws)
+    eo, pr, rt = i32(E + 1), i32(T, K), i32(T * K)
+    xd = torch.empty(T * K, d, dtype=torch.bfloat16, device="cuda")
+    smoe.smoe_dispatch(desc, idx, eo, pr, rt, ws, x_src=x, x_disp=xd)
+    yd = torch.empty_like(xd)
+    ysh = torch.empty(S, T, d, dtype=torch.bfloat16, device="cuda") if S else None
+    smoe.smoe_expert_ffn(desc, xd, eo, w1, w3, w2, yd, ws, x=x, y_shared=ysh)
+    smoe.smoe_get_status(ws)
+    torch.cuda.synchronize()
+    eo_n, rt_n = to_np(eo), to_np(rt)
+    xn = to_np(x).astype(np.float64)
+    W = [tuple(to_np(m[e]).astype(np.float64) for m in (w1, w3, w2)) for e in range(E + S)]
+    ref = np.zeros((T * K, d))
+    for e in range(E):
+        lo, hi = eo_n[e], eo_n[e + 1]
+        ref[lo:hi] = O.swiglu_ffn(xn[rt_n[lo:hi]], *W[e])
+    assert rel_err_rows(to_np(yd), ref).max() <= VALUE_TOL
+    for j in range(S):
+        assert rel_err_rows(to_np(ysh[j]), O.swiglu_ffn(xn, *W[E + j])).max() <= VALUE_TOL
