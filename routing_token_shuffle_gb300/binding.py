@@ -72,10 +72,12 @@ SIGNATURES = {
 _lib = None
 
 
-def lib(path: str = LIB_PATH):
-    """Load libsmoe.so once; raise if it is missing (no fallback path exists)."""
+def lib(path: str | None = None):
+    """Load libsmoe.so once (from ``path``, else LIB_PATH); raise if it is missing (no
+    fallback path exists)."""
     global _lib
     if _lib is None:
+        path = path or LIB_PATH
         if not os.path.exists(path):
             raise RuntimeError(f"{path} is not built; run routing_token_shuffle_gb300.build.build()")
         L = ctypes.CDLL(path)
