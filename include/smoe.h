@@ -174,11 +174,12 @@ SMOE_API int smoe_lar(const smoe_desc* desc, const int32_t* topk_idx, const int3
  *   expert_off [E+1] int32: expert e owns rows [expert_off[e], expert_off[e+1])
  *   pair_row   [T, K] int32: row of pair (t, k)
  *   row_token  [T K] int32: token of each row
+ *   row_slot   nullable [T K] int32: row of x_src feeding each row (its token's slot)
  *   x_disp     nullable [T K, d] dtype: x_disp[pair_row[t,k]] = x[t]               */
 SMOE_API int smoe_dispatch(const smoe_desc* desc, const int32_t* topk_idx,
                            const int32_t* shuf_perm, const void* x_src, int32_t* expert_off,
-                           int32_t* pair_row, int32_t* row_token, void* x_disp, void* ws,
-                           size_t ws_bytes, void* stream);
+                           int32_t* pair_row, int32_t* row_token, int32_t* row_slot,
+                           void* x_disp, void* ws, size_t ws_bytes, void* stream);
 
 /* a7/a8 -- grouped SwiGLU expert FFN: for every expert e and each of its rows,
  * y = (silu(x W1_e^T) * (x W3_e^T)) W2_e^T, bf16/tf32 tensor-core products with fp32

@@ -54,7 +54,7 @@ SIGNATURES = {
     "smoe_predict_shuffle": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "smoe_predict_shuffle_noalloc": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "smoe_lar": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _SZ, _P]),
-    "smoe_dispatch": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "smoe_dispatch": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "smoe_expert_ffn": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "smoe_combine": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "smoe_layer_forward": (ctypes.c_int, [_D, ctypes.POINTER(LayerWeights),
@@ -165,10 +165,11 @@ def smoe_lar(desc, topk_idx, expert_part, counts, ws, src_part=None, stream=None
 
 
 def smoe_dispatch(desc, topk_idx, expert_off, pair_row, row_token, ws, shuf_perm=None, x_src=None,
-                  x_disp=None, stream=None):
+                  x_disp=None, row_slot=None, stream=None):
     _check(lib().smoe_dispatch(ctypes.byref(desc), _ptr(topk_idx), _ptr(shuf_perm), _ptr(x_src),
-                               _ptr(expert_off), _ptr(pair_row), _ptr(row_token), _ptr(x_disp),
-                               _ptr(ws), ws.numel(), _stream(stream)), "smoe_dispatch")
+                               _ptr(expert_off), _ptr(pair_row), _ptr(row_token), _ptr(row_slot),
+                               _ptr(x_disp), _ptr(ws), ws.numel(), _stream(stream)),
+           "smoe_dispatch")
 
 
 def smoe_expert_ffn(desc, x_disp, expert_off, w1, w3, w2, y_disp, ws, x=None, y_shared=None,

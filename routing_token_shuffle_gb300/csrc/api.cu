@@ -258,14 +258,15 @@ SMOE_API int smoe_lar(const smoe_desc* desc, const int32_t* topk_idx, const int3
 
 SMOE_API int smoe_dispatch(const smoe_desc* desc, const int32_t* topk_idx,
                            const int32_t* shuf_perm, const void* x_src, int32_t* expert_off,
-                           int32_t* pair_row, int32_t* row_token, void* x_disp, void* ws,
-                           size_t ws_bytes, void* stream) {
+                           int32_t* pair_row, int32_t* row_token, int32_t* row_slot,
+                           void* x_disp, void* ws, size_t ws_bytes, void* stream) {
   SMOE_CHECK(check_desc(desc));
   SMOE_PTR(topk_idx);
   SMOE_OPT_PTR(shuf_perm);
   SMOE_PTR(expert_off);
   SMOE_PTR(pair_row);
   SMOE_PTR(row_token);
+  SMOE_OPT_PTR(row_slot);
   SMOE_OPT_PTR(x_disp);
   if (x_disp) SMOE_PTR(x_src);
   SMOE_CHECK(check_ws(desc, ws, ws_bytes));
@@ -276,7 +277,7 @@ SMOE_API int smoe_dispatch(const smoe_desc* desc, const int32_t* topk_idx,
     return SMOE_OK;
   }
   cudaError_t e = launch_dispatch(*desc, topk_idx, shuf_perm, x_src, expert_off, pair_row,
-                                  row_token, x_disp, ws, s);
+                                  row_token, row_slot, x_disp, ws, s);
   if (e != cudaSuccess) return cuda_fail(e, "dispatch launch");
   return SMOE_OK;
 }
@@ -341,7 +342,6 @@ static int layer_forward_impl(const smoe_desc* d, const smoe_layer_weights* W,
   void* x_disp = ws_ptr<char>(ws, L.x_disp);
   void* y_disp = ws_ptr<char>(ws, L.y_disp);
   void* y_sh = d->n_shared ? ws_ptr<char>(ws, L.y_sh) : nullptr;
-  (void)TK;
 
   cudaError_t e = launch_route(*d, d->T, io->x, W->w_gate, nullptr, logits, idx, w, ws, s);
   if (e != cudaSuccess) return cuda_fail(e, "route launch");
@@ -354,7 +354,7 @@ static int layer_forward_impl(const smoe_desc* d, const smoe_layer_weights* W,
   }
   const void* x_src = io->skip_shuffle ? io->x : x_shuf;
   e = launch_dispatch(*d, idx, io->skip_shuffle ? nullptr : perm, x_src, expert_off, pair_row,
-                      row_token, x_disp, ws, s);
+                      row_token, nullptr, x_disp, ws, s);
   if (e != cudaSuccess) return cuda_fail(e, "dispatch launch");
   e = launch_expert_ffn(*d, x_disp, io->x, expert_off, W->w1, W->w3, W->w2, y_disp, y_sh, ws, s);
   if (e != cudaSuccess) return cuda_fail(e, "expert ffn launch");

@@ -126,9 +126,12 @@ cudaError_t launch_lar(const smoe_desc& d, const int32_t* idx, const int32_t* sr
                        const int32_t* emap, unsigned long long* counts, void* ws,
                        cudaStream_t s);
 
+// row_slot: nullable output [T K], the x_src row of each dispatched row (the workspace
+// keeps it when NULL).
 cudaError_t launch_dispatch(const smoe_desc& d, const int32_t* idx, const int32_t* perm,
                             const void* x_src, int32_t* expert_off, int32_t* pair_row,
-                            int32_t* row_token, void* x_disp, void* ws, cudaStream_t s);
+                            int32_t* row_token, int32_t* row_slot, void* x_disp, void* ws,
+                            cudaStream_t s);
 
 cudaError_t launch_expert_ffn(const smoe_desc& d, const void* x_disp, const void* x,
                               const int32_t* expert_off, const void* w1, const void* w3,

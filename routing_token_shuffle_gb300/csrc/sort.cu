@@ -415,15 +415,17 @@ cudaError_t launch_predict_shuffle(const smoe_desc& d, const int32_t* ids, const
 
 cudaError_t launch_dispatch(const smoe_desc& d, const int32_t* idx, const int32_t* perm,
                             const void* x_src, int32_t* expert_off, int32_t* pair_row,
-                            int32_t* row_token, void* x_disp, void* ws, cudaStream_t s) {
+                            int32_t* row_token, int32_t* row_slot, void* x_disp, void* ws,
+                            cudaStream_t s) {
   WsLayout L;
   ws_layout(d, &L);
   DeviceStatus* st = ws_ptr<DeviceStatus>(ws, L.status);
   int32_t* hist = ws_ptr<int32_t>(ws, L.sort_hist);
   int32_t* offs = ws_ptr<int32_t>(ws, L.sort_off);
-  int32_t* row_src = ws_ptr<int32_t>(ws, L.row_src);
-  // the per-pair bucket reuses the row_src slot's twin: pair buckets live after row_src
-  int32_t* bucket = row_src + (size_t)d.T * d.K;
+  int32_t* ws_rows = ws_ptr<int32_t>(ws, L.row_src);
+  int32_t* row_src = row_slot ? row_slot : ws_rows;
+  // per-pair buckets live in the second half of the workspace's row-source region
+  int32_t* bucket = ws_rows + (size_t)d.T * d.K;
   const int n = d.T * d.K;
   const int ntiles = ceil_div(n, kSortTile);
   SMOE_COUNT_LAUNCH(1);

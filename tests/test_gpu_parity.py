@@ -187,14 +187,17 @@ def test_dispatch(name, T):
     logits, idx, w = run_route(c, desc, ws)
     pred, perm, off, xs = run_shuffle(c, desc, ws)
     TK = cfg.T * cfg.K
-    eo, pr, rt = i32(cfg.E + 1), i32(cfg.T, cfg.K), i32(TK)
+    eo, pr, rt, rs = i32(cfg.E + 1), i32(cfg.T, cfg.K), i32(TK), i32(TK)
     xd = torch.empty(TK, cfg.d, dtype=c.x.dtype, device="cuda")
-    smoe.smoe_dispatch(desc, idx, eo, pr, rt, ws, shuf_perm=perm, x_src=xs, x_disp=xd)
+    smoe.smoe_dispatch(desc, idx, eo, pr, rt, ws, shuf_perm=perm, x_src=xs, x_disp=xd, row_slot=rs)
     smoe.smoe_get_status(ws)
     r_eo, r_pr, r_rt = O.expert_dispatch(to_np(idx), cfg.E, to_np(perm))
     assert np.array_equal(to_np(eo), r_eo)
     assert np.array_equal(to_np(pr), r_pr)
     assert np.array_equal(to_np(rt), r_rt)
+    slot_of = np.empty(cfg.T, np.int64)
+    slot_of[to_np(perm)] = np.arange(cfg.T)
+    assert np.array_equal(to_np(rs), slot_of[r_rt])          # row -> slot of its token
     assert torch.equal(xd, c.x[torch.as_tensor(r_rt, device="cuda").long()])
     # without the shuffle: token order, source rows straight from x
     smoe.smoe_dispatch(desc, idx, eo, pr, rt, ws, x_src=c.x, x_disp=xd)
