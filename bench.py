@@ -407,25 +407,38 @@ def run_native(args):
     value = whole_job_rate(cfg.T * args.steps, world, total_ms_max / 1e3)
     smoe.smoe_get_status(wl.ws)
 
-    # end to end through the host-buffer entry point: H2D of x and ids, D2H of y
-    xh = wl.x.cpu().pin_memory()
-    ih = torch.as_tensor(wl.ids).pin_memory()
-    yh = torch.empty_like(xh).pin_memory()
-    for _ in range(2):
-        smoe.smoe_layer_forward_host(wl.desc, wl.weights, xh, ih, yh, wl.ws)
+    # end to end through the host-buffer entry point (H2D of x and ids, the layer, D2H of
+    # y every step), pipelined the way a serving loop would: two streams and two
+    # workspaces in turn, so one step's copies overlap the other's kernels
+    xh = [wl.x.cpu().pin_memory() for _ in range(2)]
+    ih = [torch.as_tensor(wl.ids).pin_memory() for _ in range(2)]
+    yh = [torch.empty_like(xh[0]).pin_memory() for _ in range(2)]
+    streams = [torch.cuda.current_stream(), torch.cuda.Stream()]
+    wss = [wl.ws, smoe.workspace(wl.desc, dev)]
+
+    def e2e_step(i):
+        j = i & 1
+        smoe.smoe_layer_forward_host(wl.desc, wl.weights, xh[j], ih[j], yh[j], wss[j],
+                                     stream=streams[j])
+
+    for i in range(4):
+        e2e_step(i)
     torch.cuda.synchronize()
     barrier(active)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.steps):
-        smoe.smoe_layer_forward_host(wl.desc, wl.weights, xh, ih, yh, wl.ws)
-    e1.record()
+    e0.record(streams[0])
+    streams[1].wait_event(e0)
+    for i in range(args.steps):
+        e2e_step(i)
+    streams[0].wait_stream(streams[1])
+    e1.record(streams[0])
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), active, device=dev)
+    del wss
     e2e_value = whole_job_rate(cfg.T * args.steps, world, e2e_ms / 1e3)
-    h2d = xh.numel() * xh.element_size() + ih.numel() * ih.element_size()
-    d2h = yh.numel() * yh.element_size()
+    h2d = xh[0].numel() * xh[0].element_size() + ih[0].numel() * ih[0].element_size()
+    d2h = yh[0].numel() * yh[0].element_size()
 
     # roofline of the dominant kernel: the grouped expert FFN GEMMs. Its bound follows
     # from its arithmetic intensity against the measured ridge point (decode-sized

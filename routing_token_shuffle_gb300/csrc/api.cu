@@ -148,7 +148,9 @@ bool ws_layout(const smoe_desc& d, WsLayout* L) {
   L->pf_qs = take(2 * T * dm * b);
   L->pf_logits = take(4 * 2 * T * E);
   L->pf_idx = take(4 * 2 * T * K);
-  L->route_part = take(4 * (size_t)route_splits(d, d.T) * T * E);
+  // the prefetch predictor routes 2T rows in one launch
+  L->route_part = take(4 * E * std::max((size_t)route_splits(d, d.T) * T,
+                                        (size_t)route_splits(d, 2 * d.T) * 2 * T));
   L->total = off;
   return true;
 }
@@ -461,11 +463,10 @@ SMOE_API int smoe_prefetch_predict(const smoe_desc* desc, const float* r, const 
   const size_t T = desc->T;
   cudaError_t e = launch_prefetch_ln(*desc, r, d_l, y, gamma, beta, qs, s);
   if (e != cudaSuccess) return cuda_fail(e, "prefetch layernorm launch");
-  e = launch_route(*desc, desc->T, qs, w_gate_next, nullptr, logits_q ? logits_q : lg, pred_idx,
-                   wq, ws, s);
-  if (e != cudaSuccess) return cuda_fail(e, "prefetch route launch");
-  e = launch_route(*desc, desc->T, qs + T * desc->d * elem_size(*desc), w_gate_next, nullptr,
-                   logits_s ? logits_s : lg + T * desc->E, true_idx, wq + T * desc->K, ws, s);
+  // q rows [0, T) and s rows [T, 2T) in one routing launch
+  (void)lg;
+  e = launch_route(*desc, 2 * desc->T, qs, w_gate_next, nullptr, logits_q, pred_idx, wq, ws, s,
+                   RouteSplitOut{desc->T, logits_s, true_idx, wq + T * desc->K});
   if (e != cudaSuccess) return cuda_fail(e, "prefetch route launch");
   e = launch_hits(*desc, pred_idx, true_idx, hits, s);
   if (e != cudaSuccess) return cuda_fail(e, "hits launch");

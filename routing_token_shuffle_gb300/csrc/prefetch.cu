@@ -10,7 +10,6 @@ namespace smoe {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kMaxChunks = 8;  // 4-element chunks per thread: d <= 8192
 
 __device__ __forceinline__ float2 block_sum2(float2 v, float2* red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -52,7 +51,7 @@ __device__ __forceinline__ void store4(__nv_bfloat16* p, const float* v) {
 // Row t: q = LN(d_l + r_t) -> qs[t], s = LN(r_t + y_t) -> qs[T + t]; biased variance,
 // eps 1e-5, two passes over values held in registers (4-element chunks), output
 // rounded to TE.
-template <typename TE>
+template <typename TE, int kMaxChunks>
 __global__ void __launch_bounds__(kThreads)
 ln_pair_kernel(const float* __restrict__ r, const float* __restrict__ d_l,
                const TE* __restrict__ y, const float* __restrict__ gamma,
@@ -142,17 +141,33 @@ hits_kernel(const int32_t* __restrict__ pred, const int32_t* __restrict__ truth,
 
 }  // namespace
 
+template <typename TE, int kChunks>
+void ln_launch(const smoe_desc& d, const float* r, const float* d_l, const void* y,
+               const float* gamma, const float* beta, void* qs, cudaStream_t s) {
+  SMOE_COUNT_LAUNCH(1);
+  ln_pair_kernel<TE, kChunks><<<d.T, kThreads, 0, s>>>(r, d_l, static_cast<const TE*>(y), gamma,
+                                                       beta, static_cast<TE*>(qs), d.T, d.d);
+}
+
+// One CTA per token; the per-thread register arrays are sized to the 4-element chunks the
+// row needs (d <= 1024 chunks * 4), which keeps several CTAs resident per SM.
+template <typename TE>
+void ln_dispatch(const smoe_desc& d, const float* r, const float* d_l, const void* y,
+                 const float* gamma, const float* beta, void* qs, cudaStream_t s) {
+  const int chunks = ceil_div(d.d, 4 * kThreads);
+  if (chunks <= 1) ln_launch<TE, 1>(d, r, d_l, y, gamma, beta, qs, s);
+  else if (chunks <= 2) ln_launch<TE, 2>(d, r, d_l, y, gamma, beta, qs, s);
+  else if (chunks <= 4) ln_launch<TE, 4>(d, r, d_l, y, gamma, beta, qs, s);
+  else ln_launch<TE, 8>(d, r, d_l, y, gamma, beta, qs, s);
+}
+
 cudaError_t launch_prefetch_ln(const smoe_desc& d, const float* r, const float* d_l,
                                const void* y, const float* gamma, const float* beta, void* qs,
                                cudaStream_t s) {
-  SMOE_COUNT_LAUNCH(1);
   if (d.dtype == SMOE_F32)
-    ln_pair_kernel<float><<<d.T, kThreads, 0, s>>>(r, d_l, static_cast<const float*>(y), gamma,
-                                                   beta, static_cast<float*>(qs), d.T, d.d);
+    ln_dispatch<float>(d, r, d_l, y, gamma, beta, qs, s);
   else
-    ln_pair_kernel<__nv_bfloat16><<<d.T, kThreads, 0, s>>>(
-        r, d_l, static_cast<const __nv_bfloat16*>(y), gamma, beta,
-        static_cast<__nv_bfloat16*>(qs), d.T, d.d);
+    ln_dispatch<__nv_bfloat16>(d, r, d_l, y, gamma, beta, qs, s);
   return cudaGetLastError();
 }
 

@@ -28,10 +28,18 @@ template <int kMaxPerLane>
 __global__ void __launch_bounds__(kSelWarps * 32)
 select_kernel(const float* __restrict__ part, int KS, long long split_stride,
               float* __restrict__ logits_out, int T, int E, int K, int H, int renorm,
-              int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+              int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, RouteSplitOut so) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kSelWarps + (threadIdx.x >> 5);
   if (t >= T) return;
+  // rows from so.split on go to the second output set, renumbered from 0
+  const bool second = t >= so.split;
+  const int to = second ? t - so.split : t;
+  if (second) {
+    logits_out = so.logits;
+    topk_idx = so.idx;
+    topk_w = so.w;
+  }
   float v[kMaxPerLane];
   float m = -INFINITY;
 #pragma unroll
@@ -42,7 +50,7 @@ select_kernel(const float* __restrict__ part, int KS, long long split_stride,
       const float* p = part + (size_t)t * E + e;
       acc = p[0];
       for (int s = 1; s < KS; ++s) acc += p[(size_t)s * split_stride];
-      if (logits_out) logits_out[(size_t)t * E + e] = acc;
+      if (logits_out) logits_out[(size_t)to * E + e] = acc;
     }
     v[i] = acc;
     m = fmaxf(m, acc);
@@ -93,8 +101,8 @@ select_kernel(const float* __restrict__ part, int KS, long long split_stride,
     my_w = my_w / s;
   }
   if (lane < K) {
-    topk_idx[(size_t)t * K + lane] = my_idx;
-    topk_w[(size_t)t * K + lane] = my_w;
+    topk_idx[(size_t)to * K + lane] = my_idx;
+    topk_w[(size_t)to * K + lane] = my_w;
   }
 }
 
@@ -301,7 +309,7 @@ int route_splits(const smoe_desc& d, int rows) {
 
 cudaError_t launch_route(const smoe_desc& d, int rows, const void* x, const void* w_gate,
                          const float* logits_in, float* logits_out, int32_t* topk_idx,
-                         float* topk_w, void* ws, cudaStream_t s) {
+                         float* topk_w, void* ws, cudaStream_t s, RouteSplitOut so) {
   const float* part = logits_in;
   int KS = 1;
   if (!logits_in) {
@@ -351,13 +359,13 @@ cudaError_t launch_route(const smoe_desc& d, int rows, const void* x, const void
   SMOE_COUNT_LAUNCH(1);
   if (d.E <= 128)
     select_kernel<4><<<grid, block, 0, s>>>(part, KS, stride, lo, rows, d.E, d.K, d.H, d.renorm,
-                                            topk_idx, topk_w);
+                                            topk_idx, topk_w, so);
   else if (d.E <= 256)
     select_kernel<8><<<grid, block, 0, s>>>(part, KS, stride, lo, rows, d.E, d.K, d.H, d.renorm,
-                                            topk_idx, topk_w);
+                                            topk_idx, topk_w, so);
   else
     select_kernel<16><<<grid, block, 0, s>>>(part, KS, stride, lo, rows, d.E, d.K, d.H, d.renorm,
-                                             topk_idx, topk_w);
+                                             topk_idx, topk_w, so);
   return cudaGetLastError();
 }
 

@@ -113,9 +113,19 @@ extern thread_local unsigned long long g_kernel_launches;
 // Each returns cudaSuccess or the launch error; shapes are validated by the caller.
 int route_splits(const smoe_desc& d, int rows);  // K splits of the tensor-core gate GEMM
 
+// Rows from `split` on write their logits / indices / weights to these outputs instead,
+// renumbered from 0 (one routing launch serves two row sets).
+struct RouteSplitOut {
+  int split;
+  float* logits;
+  int32_t* idx;
+  float* w;
+};
+
 cudaError_t launch_route(const smoe_desc& d, int rows, const void* x, const void* w_gate,
                          const float* logits_in, float* logits_out, int32_t* topk_idx,
-                         float* topk_w, void* ws, cudaStream_t s);
+                         float* topk_w, void* ws, cudaStream_t s,
+                         RouteSplitOut so = RouteSplitOut{0x7fffffff, nullptr, nullptr, nullptr});
 
 cudaError_t launch_predict_shuffle(const smoe_desc& d, const int32_t* ids, const float* conf,
                                    const int32_t* emap, const void* x, int32_t* pred,
