@@ -16,6 +16,7 @@ __global__ void __launch_bounds__(kThreads)
 combine_kernel(const uint4* __restrict__ y_disp, const int32_t* __restrict__ pair_row,
                const float* __restrict__ w, const uint4* __restrict__ y_sh, uint4* __restrict__ y,
                int T, int K, int S, int nvec, int nrows, DeviceStatus* st) {
+  pdl_wait_and_trigger();
   constexpr int V = Elem<TE>::kPerVec16;
   __shared__ int s_row[32];
   __shared__ float s_w[32];
@@ -63,13 +64,12 @@ cudaError_t launch_combine(const smoe_desc& d, const void* y_disp, const int32_t
   DeviceStatus* st = ws_ptr<DeviceStatus>(ws, L.status);
   const int nvec = (int)(d.d * elem_size(d) / 16);
   const int S = y_sh ? d.n_shared : 0;
-  SMOE_COUNT_LAUNCH(1);
   if (d.dtype == SMOE_F32)
-    combine_kernel<float><<<d.T, kThreads, 0, s>>>(
-        static_cast<const uint4*>(y_disp), pair_row, w, static_cast<const uint4*>(y_sh),
-        static_cast<uint4*>(y), d.T, d.K, S, nvec, d.T * d.K, st);
+    SMOE_LAUNCH(combine_kernel<float>, d.T, kThreads, 0, s, static_cast<const uint4*>(y_disp),
+        pair_row, w, static_cast<const uint4*>(y_sh), static_cast<uint4*>(y), d.T, d.K, S, nvec,
+        d.T * d.K, st);
   else
-    combine_kernel<__nv_bfloat16><<<d.T, kThreads, 0, s>>>(
+    SMOE_LAUNCH(combine_kernel<__nv_bfloat16>, d.T, kThreads, 0, s,
         static_cast<const uint4*>(y_disp), pair_row, w, static_cast<const uint4*>(y_sh),
         static_cast<uint4*>(y), d.T, d.K, S, nvec, d.T * d.K, st);
   return cudaGetLastError();

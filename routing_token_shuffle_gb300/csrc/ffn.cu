@@ -43,6 +43,7 @@ constexpr size_t kSmemBytes =
 __global__ void tile_table_kernel(const int32_t* __restrict__ expert_off, int E, int n_shared,
                                   int T, int TK, int bm, int32_t* __restrict__ tile_start,
                                   DeviceStatus* st) {
+  pdl_wait_and_trigger();
   const int lane = threadIdx.x;
   const int G = E + n_shared;
   bool bad = false;
@@ -136,6 +137,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmA_sh,
                     const __grid_constant__ CUtensorMap tmB1,
                     const __grid_constant__ CUtensorMap tmB3, const GemmArgs p) {
+  pdl_wait_and_trigger();
   using TE = typename std::conditional<F32, float, __nv_bfloat16>::type;
   constexpr int BK = F32 ? 32 : 64;           // elements per 128-byte row
   constexpr int kMmaK = F32 ? 8 : 16;          // elements per MMA
@@ -380,6 +382,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmA_sh,
                          const __grid_constant__ CUtensorMap tmB1,
                          const __grid_constant__ CUtensorMap tmB3, const GemmArgs p) {
+  pdl_wait_and_trigger();
   using TE = __nv_bfloat16;
   constexpr uint32_t kIdesc = tc::instr_desc(false, 256, 256);
 
@@ -578,8 +581,7 @@ cudaError_t launch_gemm(const CUtensorMap& A, const CUtensorMap& Ash, const CUte
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = (int)std::min<long long>(sm_count(), std::max<long long>(tile_bound, 1));
-  SMOE_COUNT_LAUNCH(1);
-  kern<<<grid, kThreads, kSmemBytes, s>>>(A, Ash, B1, B3, args);
+  SMOE_LAUNCH(kern, grid, kThreads, kSmemBytes, s, A, Ash, B1, B3, args);
   return cudaGetLastError();
 }
 
@@ -597,13 +599,15 @@ cudaError_t launch_gemm_pair(const CUtensorMap& A, const CUtensorMap& Ash, const
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kPairSmemBytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   SMOE_COUNT_LAUNCH(1);
   return cudaLaunchKernelEx(&cfg, kern, A, Ash, B1, B3, args);
 }
@@ -627,8 +631,7 @@ cudaError_t run_ffn(const smoe_desc& d, const void* x_disp, const void* x,
   const uint32_t box_k = F32 ? 32 : 64;
   const bool pairs = !F32 && use_pair_tiles(d);
   const int bm = pairs ? 256 : kBM;
-  SMOE_COUNT_LAUNCH(1);
-  tile_table_kernel<<<1, 32, 0, s>>>(expert_off, d.E, d.n_shared, d.T, TK, bm, tiles, st);
+  SMOE_LAUNCH(tile_table_kernel, 1, 32, 0, s, expert_off, d.E, d.n_shared, d.T, TK, bm, tiles, st);
 
   const long long mtile_bound =
       ceil_div(TK, bm) + d.E + (long long)d.n_shared * ceil_div(d.T, bm);

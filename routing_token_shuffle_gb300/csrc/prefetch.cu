@@ -56,6 +56,7 @@ __global__ void __launch_bounds__(kThreads)
 ln_pair_kernel(const float* __restrict__ r, const float* __restrict__ d_l,
                const TE* __restrict__ y, const float* __restrict__ gamma,
                const float* __restrict__ beta, TE* __restrict__ qs, int T, int d) {
+  pdl_wait_and_trigger();
   __shared__ float2 red[kThreads / 32];
   const int t = blockIdx.x;
   const float* rr = r + (size_t)t * d;
@@ -118,6 +119,7 @@ ln_pair_kernel(const float* __restrict__ r, const float* __restrict__ d_l,
 __global__ void __launch_bounds__(kThreads)
 hits_kernel(const int32_t* __restrict__ pred, const int32_t* __restrict__ truth, int T, int K,
             unsigned long long* __restrict__ hits) {
+  pdl_wait_and_trigger();
   __shared__ unsigned long long red[kThreads / 32];
   unsigned long long c = 0;
   for (int t = blockIdx.x * kThreads + threadIdx.x; t < T; t += gridDim.x * kThreads) {
@@ -142,33 +144,33 @@ hits_kernel(const int32_t* __restrict__ pred, const int32_t* __restrict__ truth,
 }  // namespace
 
 template <typename TE, int kChunks>
-void ln_launch(const smoe_desc& d, const float* r, const float* d_l, const void* y,
+cudaError_t ln_launch(const smoe_desc& d, const float* r, const float* d_l, const void* y,
                const float* gamma, const float* beta, void* qs, cudaStream_t s) {
-  SMOE_COUNT_LAUNCH(1);
-  ln_pair_kernel<TE, kChunks><<<d.T, kThreads, 0, s>>>(r, d_l, static_cast<const TE*>(y), gamma,
-                                                       beta, static_cast<TE*>(qs), d.T, d.d);
+  {
+    auto kfn_ = ln_pair_kernel<TE, kChunks>;
+    SMOE_LAUNCH(kfn_, d.T, kThreads, 0, s, r, d_l, static_cast<const TE*>(y), gamma, beta,
+        static_cast<TE*>(qs), d.T, d.d);
+  }
+  return cudaSuccess;
 }
 
 // One CTA per token; the per-thread register arrays are sized to the 4-element chunks the
 // row needs (d <= 1024 chunks * 4), which keeps several CTAs resident per SM.
 template <typename TE>
-void ln_dispatch(const smoe_desc& d, const float* r, const float* d_l, const void* y,
+cudaError_t ln_dispatch(const smoe_desc& d, const float* r, const float* d_l, const void* y,
                  const float* gamma, const float* beta, void* qs, cudaStream_t s) {
   const int chunks = ceil_div(d.d, 4 * kThreads);
-  if (chunks <= 1) ln_launch<TE, 1>(d, r, d_l, y, gamma, beta, qs, s);
-  else if (chunks <= 2) ln_launch<TE, 2>(d, r, d_l, y, gamma, beta, qs, s);
-  else if (chunks <= 4) ln_launch<TE, 4>(d, r, d_l, y, gamma, beta, qs, s);
-  else ln_launch<TE, 8>(d, r, d_l, y, gamma, beta, qs, s);
+  if (chunks <= 1) return ln_launch<TE, 1>(d, r, d_l, y, gamma, beta, qs, s);
+  if (chunks <= 2) return ln_launch<TE, 2>(d, r, d_l, y, gamma, beta, qs, s);
+  if (chunks <= 4) return ln_launch<TE, 4>(d, r, d_l, y, gamma, beta, qs, s);
+  return ln_launch<TE, 8>(d, r, d_l, y, gamma, beta, qs, s);
 }
 
 cudaError_t launch_prefetch_ln(const smoe_desc& d, const float* r, const float* d_l,
                                const void* y, const float* gamma, const float* beta, void* qs,
                                cudaStream_t s) {
-  if (d.dtype == SMOE_F32)
-    ln_dispatch<float>(d, r, d_l, y, gamma, beta, qs, s);
-  else
-    ln_dispatch<__nv_bfloat16>(d, r, d_l, y, gamma, beta, qs, s);
-  return cudaGetLastError();
+  if (d.dtype == SMOE_F32) return ln_dispatch<float>(d, r, d_l, y, gamma, beta, qs, s);
+  return ln_dispatch<__nv_bfloat16>(d, r, d_l, y, gamma, beta, qs, s);
 }
 
 cudaError_t launch_hits(const smoe_desc& d, const int32_t* pred_idx, const int32_t* true_idx,
@@ -176,8 +178,7 @@ cudaError_t launch_hits(const smoe_desc& d, const int32_t* pred_idx, const int32
   cudaError_t e = cudaMemsetAsync(hits, 0, sizeof(unsigned long long), s);
   if (e != cudaSuccess) return e;
   const int grid = std::max(1, std::min(ceil_div(d.T, kThreads), 1024));
-  SMOE_COUNT_LAUNCH(1);
-  hits_kernel<<<grid, kThreads, 0, s>>>(pred_idx, true_idx, d.T, d.K, hits);
+  SMOE_LAUNCH(hits_kernel, grid, kThreads, 0, s, pred_idx, true_idx, d.T, d.K, hits);
   return cudaGetLastError();
 }
 

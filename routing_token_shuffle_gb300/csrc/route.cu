@@ -29,6 +29,7 @@ __global__ void __launch_bounds__(kSelWarps * 32)
 select_kernel(const float* __restrict__ part, int KS, long long split_stride,
               float* __restrict__ logits_out, int T, int E, int K, int H, int renorm,
               int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, RouteSplitOut so) {
+  pdl_wait_and_trigger();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kSelWarps + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -113,6 +114,7 @@ constexpr int kBM = 64, kBN = 64, kBK = 32;
 __global__ void __launch_bounds__(256)
 gate_gemm_f32_kernel(const float* __restrict__ x, const float* __restrict__ wg,
                      float* __restrict__ logits, int rows, int d, int E) {
+  pdl_wait_and_trigger();
   __shared__ float xs[kBK][kBM + 4];
   __shared__ float gs[kBK][kBN + 4];
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
@@ -172,6 +174,7 @@ struct GateArgs {
 __global__ void __launch_bounds__(256, 1)
 gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                const GateArgs p) {
+  pdl_wait_and_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -319,10 +322,8 @@ cudaError_t launch_route(const smoe_desc& d, int rows, const void* x, const void
     part = pbuf;
     if (d.dtype == SMOE_F32) {
       dim3 grid(ceil_div(rows, kBM), ceil_div(d.E, kBN));
-      SMOE_COUNT_LAUNCH(1);
-      gate_gemm_f32_kernel<<<grid, 256, 0, s>>>(static_cast<const float*>(x),
-                                                static_cast<const float*>(w_gate), pbuf, rows,
-                                                d.d, d.E);
+      SMOE_LAUNCH(gate_gemm_f32_kernel, grid, 256, 0, s, static_cast<const float*>(x),
+          static_cast<const float*>(w_gate), pbuf, rows, d.d, d.E);
     } else {
       KS = route_splits(d, rows);
       const int E_pad = (d.E + 15) / 16 * 16;
@@ -349,23 +350,21 @@ cudaError_t launch_route(const smoe_desc& d, int rows, const void* x, const void
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
       dim3 grid(ceil_div(rows, 128), KS);
-      SMOE_COUNT_LAUNCH(1);
-      gate_tc_kernel<<<grid, 256, smem, s>>>(tX, tW, a);
+      SMOE_LAUNCH(gate_tc_kernel, grid, 256, smem, s, tX, tW, a);
     }
   }
   float* lo = logits_out == logits_in ? nullptr : logits_out;
   const long long stride = (long long)rows * d.E;
   const dim3 grid(ceil_div(rows, kSelWarps)), block(kSelWarps * 32);
-  SMOE_COUNT_LAUNCH(1);
   if (d.E <= 128)
-    select_kernel<4><<<grid, block, 0, s>>>(part, KS, stride, lo, rows, d.E, d.K, d.H, d.renorm,
-                                            topk_idx, topk_w, so);
+    SMOE_LAUNCH(select_kernel<4>, grid, block, 0, s, part, KS, stride, lo, rows, d.E, d.K, d.H,
+        d.renorm, topk_idx, topk_w, so);
   else if (d.E <= 256)
-    select_kernel<8><<<grid, block, 0, s>>>(part, KS, stride, lo, rows, d.E, d.K, d.H, d.renorm,
-                                            topk_idx, topk_w, so);
+    SMOE_LAUNCH(select_kernel<8>, grid, block, 0, s, part, KS, stride, lo, rows, d.E, d.K, d.H,
+        d.renorm, topk_idx, topk_w, so);
   else
-    select_kernel<16><<<grid, block, 0, s>>>(part, KS, stride, lo, rows, d.E, d.K, d.H, d.renorm,
-                                             topk_idx, topk_w, so);
+    SMOE_LAUNCH(select_kernel<16>, grid, block, 0, s, part, KS, stride, lo, rows, d.E, d.K, d.H,
+        d.renorm, topk_idx, topk_w, so);
   return cudaGetLastError();
 }
 

@@ -109,6 +109,50 @@ inline T* ws_ptr(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast
 extern thread_local unsigned long long g_kernel_launches;
 #define SMOE_COUNT_LAUNCH(n) (::smoe::g_kernel_launches += (n))
 
+// ---------------------------------------------------------------- dependent launch
+// Every library kernel is launched with programmatic stream serialisation and starts with
+// pdl_wait() (griddepcontrol.wait: the previous kernel in the stream has completed and its
+// writes are visible) before touching global memory, then pdl_trigger() so that the next
+// kernel's CTAs may be scheduled while this grid drains. Without a programmatic
+// predecessor the wait returns at once.
+__device__ __forceinline__ void pdl_wait_and_trigger() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t s, Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  SMOE_COUNT_LAUNCH(1);
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
+#define SMOE_LAUNCH(kern, grid, block, smem, stream, ...)                              \
+  do {                                                                                 \
+    cudaError_t le_ = ::smoe::launch_k(kern, dim3(grid), dim3(block), smem, stream,     \
+                                       __VA_ARGS__);                                   \
+    if (le_ != cudaSuccess) return le_;                                                \
+  } while (0)
+
+// The same for functions that return an smoe_status.
+#define SMOE_LAUNCH_STATUS(kern, grid, block, smem, stream, ...)                       \
+  do {                                                                                 \
+    cudaError_t le_ = ::smoe::launch_k(kern, dim3(grid), dim3(block), smem, stream,     \
+                                       __VA_ARGS__);                                   \
+    if (le_ != cudaSuccess)                                                            \
+      return ::smoe::set_last_error(SMOE_ERR_CUDA, cudaGetErrorString(le_));           \
+  } while (0)
+
 // ---------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error; shapes are validated by the caller.
 int route_splits(const smoe_desc& d, int rows);  // K splits of the tensor-core gate GEMM

@@ -42,6 +42,7 @@ predict_hist_kernel(const int32_t* __restrict__ ids, const float* __restrict__ c
                     const int32_t* __restrict__ emap, int T, int E, int P, int vocab,
                     int32_t* __restrict__ pred, int32_t* __restrict__ hist, int ntiles,
                     DeviceStatus* st) {
+  pdl_wait_and_trigger();
   extern __shared__ float s_rows[];          // [kPredTokens, E]
   __shared__ int s_map[kMaxBuckets];
   __shared__ int s_list[kMaxBuckets];
@@ -137,6 +138,7 @@ __global__ void __launch_bounds__(kThreads)
 dispatch_hist_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ perm, int T,
                      int K, int E, int32_t* __restrict__ bucket, int32_t* __restrict__ hist,
                      int ntiles, DeviceStatus* st) {
+  pdl_wait_and_trigger();
   __shared__ int s_cnt[kMaxBuckets];
   const int tid = threadIdx.x;
   for (int b = tid; b < E; b += kThreads) s_cnt[b] = 0;
@@ -170,6 +172,7 @@ dispatch_hist_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict_
 __global__ void __launch_bounds__(1024)
 scan_kernel(const int32_t* __restrict__ hist, int32_t* __restrict__ offs, int L, int B,
             int ntiles, int n, int32_t* __restrict__ bucket_off) {
+  pdl_wait_and_trigger();
   __shared__ int s_warp[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int per = (L + blockDim.x - 1) / blockDim.x;
@@ -220,6 +223,7 @@ scatter_kernel(const int32_t* __restrict__ bucket, int n, int B, int ntiles,
                // kDispatch
                const int32_t* __restrict__ perm_in, int T, int K, int32_t* __restrict__ pair_row,
                int32_t* __restrict__ row_token, int32_t* __restrict__ row_src) {
+  pdl_wait_and_trigger();
   __shared__ int s_run[kMaxBuckets];
   __shared__ int s_wc[kWarps][kMaxBuckets];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -274,6 +278,7 @@ __global__ void __launch_bounds__(kThreads)
 gather_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
                    const int32_t* __restrict__ map, int nrows, int nsrc, int vec_per_row,
                    DeviceStatus* st) {
+  pdl_wait_and_trigger();
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * kThreads + threadIdx.x) >> 5;
   const int nw = (gridDim.x * kThreads) >> 5;
@@ -305,6 +310,7 @@ __global__ void __launch_bounds__(kThreads)
 lar_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ src_part,
            const int32_t* __restrict__ emap, int T, int K, int E, int P, int H,
            unsigned long long* __restrict__ counts, DeviceStatus* st) {
+  pdl_wait_and_trigger();
   __shared__ int s_map[kMaxBuckets];
   __shared__ unsigned long long s_red[3][kWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -396,18 +402,14 @@ cudaError_t launch_predict_shuffle(const smoe_desc& d, const int32_t* ids, const
   e = cudaFuncSetAttribute(predict_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)predict_smem(d.E));
   if (e != cudaSuccess) return e;
-  SMOE_COUNT_LAUNCH(1);
-  predict_hist_kernel<<<ceil_div(d.T, kPredTokens), kThreads, predict_smem(d.E), s>>>(
-      ids, conf, emap, d.T, d.E, d.P, d.vocab, pred, hist, ntiles, st);
-  SMOE_COUNT_LAUNCH(1);
-  scan_kernel<<<1, 1024, 0, s>>>(hist, offs, d.P * ntiles, d.P, ntiles, d.T, part_off);
-  SMOE_COUNT_LAUNCH(1);
-  scatter_kernel<kShuffle><<<ntiles, kThreads, 0, s>>>(pred, d.T, d.P, ntiles, offs, perm,
-                                                       nullptr, 0, 0, nullptr, nullptr, nullptr);
+  SMOE_LAUNCH(predict_hist_kernel, ceil_div(d.T, kPredTokens), kThreads, predict_smem(d.E), s, ids,
+      conf, emap, d.T, d.E, d.P, d.vocab, pred, hist, ntiles, st);
+  SMOE_LAUNCH(scan_kernel, 1, 1024, 0, s, hist, offs, d.P * ntiles, d.P, ntiles, d.T, part_off);
+  SMOE_LAUNCH(scatter_kernel<kShuffle>, ntiles, kThreads, 0, s, pred, d.T, d.P, ntiles, offs, perm,
+      nullptr, 0, 0, nullptr, nullptr, nullptr);
   if (x_shuf) {
     const int vec = (int)(d.d * elem_size(d) / 16);
-    SMOE_COUNT_LAUNCH(1);
-    gather_rows_kernel<<<grid_for_rows(d.T), kThreads, 0, s>>>(
+    SMOE_LAUNCH(gather_rows_kernel, grid_for_rows(d.T), kThreads, 0, s,
         static_cast<const uint4*>(x), static_cast<uint4*>(x_shuf), perm, d.T, d.T, vec, st);
   }
   return cudaGetLastError();
@@ -428,19 +430,14 @@ cudaError_t launch_dispatch(const smoe_desc& d, const int32_t* idx, const int32_
   int32_t* bucket = ws_rows + (size_t)d.T * d.K;
   const int n = d.T * d.K;
   const int ntiles = ceil_div(n, kSortTile);
-  SMOE_COUNT_LAUNCH(1);
-  dispatch_hist_kernel<<<ntiles, kThreads, 0, s>>>(idx, perm, d.T, d.K, d.E, bucket, hist, ntiles,
-                                                   st);
-  SMOE_COUNT_LAUNCH(1);
-  scan_kernel<<<1, 1024, 0, s>>>(hist, offs, d.E * ntiles, d.E, ntiles, n, expert_off);
-  SMOE_COUNT_LAUNCH(1);
-  scatter_kernel<kDispatch><<<ntiles, kThreads, 0, s>>>(bucket, n, d.E, ntiles, offs, nullptr,
-                                                        perm, d.T, d.K, pair_row, row_token,
-                                                        row_src);
+  SMOE_LAUNCH(dispatch_hist_kernel, ntiles, kThreads, 0, s, idx, perm, d.T, d.K, d.E, bucket, hist,
+      ntiles, st);
+  SMOE_LAUNCH(scan_kernel, 1, 1024, 0, s, hist, offs, d.E * ntiles, d.E, ntiles, n, expert_off);
+  SMOE_LAUNCH(scatter_kernel<kDispatch>, ntiles, kThreads, 0, s, bucket, n, d.E, ntiles, offs,
+      nullptr, perm, d.T, d.K, pair_row, row_token, row_src);
   if (x_disp) {
     const int vec = (int)(d.d * elem_size(d) / 16);
-    SMOE_COUNT_LAUNCH(1);
-    gather_rows_kernel<<<grid_for_rows(n), kThreads, 0, s>>>(
+    SMOE_LAUNCH(gather_rows_kernel, grid_for_rows(n), kThreads, 0, s,
         static_cast<const uint4*>(x_src), static_cast<uint4*>(x_disp), row_src, n, d.T, vec, st);
   }
   return cudaGetLastError();
@@ -455,8 +452,8 @@ cudaError_t launch_lar(const smoe_desc& d, const int32_t* idx, const int32_t* sr
   cudaError_t e = cudaMemsetAsync(counts, 0, 4 * sizeof(unsigned long long), s);
   if (e != cudaSuccess) return e;
   const int grid = std::max(1, std::min(ceil_div(d.T, kThreads), 1024));
-  SMOE_COUNT_LAUNCH(1);
-  lar_kernel<<<grid, kThreads, 0, s>>>(idx, src_part, emap, d.T, d.K, d.E, d.P, d.H, counts, st);
+  SMOE_LAUNCH(lar_kernel, grid, kThreads, 0, s, idx, src_part, emap, d.T, d.K, d.E, d.P, d.H,
+      counts, st);
   return cudaGetLastError();
 }
 
@@ -545,19 +542,15 @@ extern "C" SMOE_API int smoe_predict_shuffle_noalloc(const smoe_desc* desc,
     ce = cudaFuncSetAttribute(predict_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)predict_smem(d.E));
   if (ce != cudaSuccess) return set_last_error(SMOE_ERR_CUDA, cudaGetErrorString(ce));
-  SMOE_COUNT_LAUNCH(1);
-  predict_hist_kernel<<<ceil_div(d.T, kPredTokens), kThreads, predict_smem(d.E), s>>>(
-      token_ids, conf, expert_part, d.T, d.E, d.P, d.vocab, pred_part, hist, ntiles, nullptr);
-  SMOE_COUNT_LAUNCH(1);
-  scan_kernel<<<1, 1024, 0, s>>>(hist, offs, d.P * ntiles, d.P, ntiles, d.T, part_off);
-  SMOE_COUNT_LAUNCH(1);
-  scatter_kernel<kShuffle><<<ntiles, kThreads, 0, s>>>(pred_part, d.T, d.P, ntiles, offs,
-                                                       shuf_perm, nullptr, 0, 0, nullptr, nullptr,
-                                                       nullptr);
+  SMOE_LAUNCH_STATUS(predict_hist_kernel, ceil_div(d.T, kPredTokens), kThreads, predict_smem(d.E),
+      s, token_ids, conf, expert_part, d.T, d.E, d.P, d.vocab, pred_part, hist, ntiles, nullptr);
+  SMOE_LAUNCH_STATUS(scan_kernel, 1, 1024, 0, s, hist, offs, d.P * ntiles, d.P, ntiles, d.T,
+      part_off);
+  SMOE_LAUNCH_STATUS(scatter_kernel<kShuffle>, ntiles, kThreads, 0, s, pred_part, d.T, d.P, ntiles,
+      offs, shuf_perm, nullptr, 0, 0, nullptr, nullptr, nullptr);
   if (x_shuf) {
     const int vec = (int)(d.d * elem_size(d) / 16);
-    SMOE_COUNT_LAUNCH(1);
-    gather_rows_kernel<<<grid_for_rows(d.T), kThreads, 0, s>>>(
+    SMOE_LAUNCH_STATUS(gather_rows_kernel, grid_for_rows(d.T), kThreads, 0, s,
         static_cast<const uint4*>(x), static_cast<uint4*>(x_shuf), shuf_perm, d.T, d.T, vec,
         nullptr);
   }
