@@ -34,6 +34,8 @@ Readings where the pages are silent (each is also listed in the design notes):
   R5 FoE source partition of token copy (t, h): see ``foe_source``.
   R6 shared experts: weight 1, excluded from alpha.
   R7 LayerNorm: biased variance, eps = 1e-5.
+  R8b a token's cluster at a layer is the partition holding most of its experts
+     (lower partition on ties); table A counts cluster transitions between layers.
 
 Parity pins: every function here is checked by tests/test_oracle_pins.py
 against brute force, closed forms or hand-computed fixtures.
@@ -134,6 +136,49 @@ def predict_partition(token_ids, conf, expert_part, P):
     for e in range(conf.shape[1]):
         score[:, emap[e]] = score[:, emap[e]] + rows[:, e]   # float32 + float32 -> float32
     return np.argmax(score, axis=1).astype(np.int32)
+
+
+def token_cluster(idx, expert_part, P):
+    """A token's cluster (EP partition) at one layer: the partition holding the most of
+    its routed experts, the lower partition on ties (R8b)."""
+    dst = np.asarray(expert_part, dtype=np.int64)[np.asarray(idx, dtype=np.int64)]
+    counts = np.stack([np.sum(dst == p, axis=1) for p in range(P)], axis=1)
+    return np.argmax(counts, axis=1).astype(np.int32)
+
+
+def markov_table(prev_cluster, cur_cluster, P):
+    """Table A of the 2-gram model over a token's cluster sequence [sMoE §4.1
+    inter-layer]: A[c, p] = #(tokens in cluster c at the previous layer and p at this
+    layer) / #(tokens in cluster c at the previous layer), float32; a row with no tokens
+    is uniform 1/P."""
+    prev = np.asarray(prev_cluster, dtype=np.int64)
+    cur = np.asarray(cur_cluster, dtype=np.int64)
+    counts = np.zeros((P, P), dtype=np.float64)
+    np.add.at(counts, (prev, cur), 1.0)
+    rows = counts.sum(axis=1, keepdims=True)
+    a = np.where(rows > 0, counts / np.maximum(rows, 1.0), 1.0 / P)
+    return a.astype(np.float32)
+
+
+def predict_partition_inter(token_ids, conf, expert_part, P, K, prev_cluster, table_a):
+    """Intra-layer prediction (predict_partition) and inter-layer prediction (row
+    prev_cluster[t] of table A), adopting the more confident one [sMoE §4.1: whichever
+    of the two is more confident]. Intra confidence = best partition score / K in float32
+    (the C_p row sums to K); inter confidence = the largest entry of the A row; the inter
+    prediction (its first largest entry) is adopted only when strictly more confident."""
+    ids = np.asarray(token_ids, dtype=np.int64)
+    conf = np.asarray(conf, dtype=np.float32)
+    emap = np.asarray(expert_part, dtype=np.int64)
+    rows = conf[ids]
+    score = np.zeros((len(ids), P), dtype=np.float32)
+    for e in range(conf.shape[1]):
+        score[:, emap[e]] = score[:, emap[e]] + rows[:, e]
+    pred_intra = np.argmax(score, axis=1)
+    conf_intra = score[np.arange(len(ids)), pred_intra] / np.float32(K)   # float32 division
+    a_rows = np.asarray(table_a, dtype=np.float32)[np.asarray(prev_cluster, dtype=np.int64)]
+    pred_inter = np.argmax(a_rows, axis=1)
+    conf_inter = a_rows[np.arange(len(ids)), pred_inter]
+    return np.where(conf_inter > conf_intra, pred_inter, pred_intra).astype(np.int32)
 
 
 # ----------------------------------------------------------------------------

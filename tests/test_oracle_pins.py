@@ -512,3 +512,65 @@ def test_profile_confidence_counts_and_oov():
     np.testing.assert_allclose(conf[[0, 1, 3]].sum(axis=1), 2.0)      # K per seen row
     empty = O.profile_confidence(np.zeros(0, np.int32), np.zeros((0, 2), np.int32), 3, 4, 2)
     np.testing.assert_allclose(empty, 0.5)
+
+
+# ------------------------------------------------- inter-layer predictor -----
+
+
+def test_inter_layer_golden():
+    g = load("inter_layer_hand.json")
+    emap = np.array(g["expert_part"], np.int32)
+    assert O.token_cluster(np.array(g["prev_idx"]), emap, g["P"]).tolist() == g["prev_cluster"]
+    assert O.token_cluster(np.array(g["cur_idx"]), emap, g["P"]).tolist() == g["cur_cluster"]
+    a = O.markov_table(g["prev_cluster"], g["cur_cluster"], g["P"])
+    np.testing.assert_array_equal(a, np.array(g["table_a"], np.float32))
+    conf = np.array(g["conf_rows"], np.float32)
+    ids = np.array(g["token_ids"])
+    assert O.predict_partition(ids, conf, emap, g["P"]).tolist() == g["pred_intra"]
+    for case in g["cases"]:
+        got = O.predict_partition_inter(ids, conf, emap, g["P"], g["K"],
+                                        g["query_prev_cluster"], np.array(case["table_a"]))
+        assert got.tolist() == case["pred"], case["why"]
+
+
+def test_token_cluster_brute_force():
+    rng = np.random.default_rng(21)
+    P, E, K, T = 5, 20, 6, 200
+    idx = O.topk_select(rng.standard_normal((T, E)).astype(np.float32), K)
+    emap = rng.integers(0, P, size=E).astype(np.int32)
+    got = O.token_cluster(idx, emap, P)
+    for t in range(T):
+        cnt = [0] * P
+        for k in range(K):
+            cnt[emap[idx[t, k]]] += 1
+        assert got[t] == cnt.index(max(cnt))
+
+
+def test_markov_table_rows_and_counts():
+    rng = np.random.default_rng(22)
+    P = 4
+    prev = rng.integers(0, P - 1, size=500)           # cluster P-1 never seen before
+    cur = rng.integers(0, P, size=500)
+    a = O.markov_table(prev, cur, P)
+    np.testing.assert_allclose(a.sum(axis=1), 1.0, rtol=1e-6)
+    np.testing.assert_allclose(a[P - 1], 1.0 / P)
+    for c in range(P - 1):
+        n = sum(1 for i in range(500) if prev[i] == c)
+        for p in range(P):
+            m = sum(1 for i in range(500) if prev[i] == c and cur[i] == p)
+            assert abs(a[c, p] - m / n) < 1e-6
+
+
+def test_inter_never_confident_reduces_to_intra():
+    """An all-uniform table A (confidence 1/P) never beats the intra-layer confidence
+    max_p score/K >= 1/P (C_p rows of profiled ids sum to K)."""
+    rng = np.random.default_rng(23)
+    V, E, K, P, T = 30, 12, 3, 4, 300
+    idx = O.topk_select(rng.standard_normal((V, E)).astype(np.float32), K)
+    conf = O.profile_confidence(np.arange(V), idx, V, E, K)
+    emap = (np.arange(E) % P).astype(np.int32)
+    ids = rng.integers(0, V, size=T)
+    uni = np.full((P, P), 1.0 / P, np.float32)
+    prev = rng.integers(0, P, size=T)
+    assert np.array_equal(O.predict_partition_inter(ids, conf, emap, P, K, prev, uni),
+                          O.predict_partition(ids, conf, emap, P))
