@@ -218,13 +218,13 @@ class Workload:
         n_prof = cfg.profile_tokens
         pids, px = synth.token_batch(cfg, self.emb, "profile", n_prof, dev)
         px = px.to(cfg.torch_dtype)
+        chunk = min(n_prof, 8192)
+        pdesc = smoe.desc_from_config(cfg, T=chunk)
         if prepare_with_oracle:
             import oracle as O
             _, self.profile_idx, _ = O.route(px.float().cpu().numpy(),
                                              self.w_gate.float().cpu().numpy(), cfg.K, cfg.H)
         else:
-            chunk = min(n_prof, 8192)
-            pdesc = smoe.desc_from_config(cfg, T=chunk)
             pws = smoe.workspace(pdesc, dev)
             pidx = torch.empty(n_prof, cfg.K, dtype=torch.int32, device=dev)
             pw = torch.empty(chunk, cfg.K, device=dev)
@@ -259,6 +259,29 @@ class Workload:
         self.y = torch.empty_like(self.x)
         self.weights = smoe.layer_weights(self.w_gate, self.w1, self.w3, self.w2, self.conf_d,
                                           self.emap_d)
+        # inter-layer predictor inputs: a stand-in previous layer routes the profile batch and
+        # the measured batch; table A counts cluster transitions on the profile batch
+        self.inter = None
+        if not prepare_with_oracle:
+            wprev = synth.previous_layer_gate(cfg, dev)
+            _, px2 = synth.token_batch(cfg, self.emb, "profile", n_prof, dev)
+            px2 = px2.to(cfg.torch_dtype)
+            pprev = torch.empty(n_prof, cfg.K, dtype=torch.int32, device=dev)
+            pws2 = smoe.workspace(pdesc, dev)
+            pw2 = torch.empty(chunk, cfg.K, device=dev)
+            for lo in range(0, n_prof, chunk):
+                smoe.smoe_route(pdesc, px2[lo:lo + chunk], wprev, pprev[lo:lo + chunk], pw2,
+                                ws=pws2)
+            table = profiling.transition_table(
+                profiling.cluster_of(pprev.cpu().numpy(), self.emap, cfg.P),
+                profiling.cluster_of(self.profile_idx, self.emap, cfg.P), cfg.P)
+            del px2, pws2, pw2, pprev
+            bidx = torch.empty(cfg.T, cfg.K, dtype=torch.int32, device=dev)
+            bw = torch.empty(cfg.T, cfg.K, device=dev)
+            smoe.smoe_route(self.desc, self.x, wprev, bidx, bw, ws=self.ws)
+            prev_cluster = torch.empty(cfg.T, dtype=torch.int32, device=dev)
+            smoe.smoe_token_cluster(self.desc, bidx, self.emap_d, prev_cluster, self.ws)
+            self.inter = dict(prev=prev_cluster, table=torch.as_tensor(table, device=dev))
         self.prefetch = None
         if cfg.prefetch and not prepare_with_oracle:
             r, wgn, gamma, beta = synth.predictor_inputs(cfg, dev)
@@ -486,6 +509,25 @@ def run_native(args):
                "sample": f"first {n} of the {cfg.T} tokens of this workload's batch, the whole "
                          f"layer in float64 numpy ({secs:.1f} s)"}
     lar = wl.lar.cpu().numpy()
+    inter_info = None
+    if wl.inter is not None:
+        pred_i = torch.empty_like(wl.pred)
+        perm_i = torch.empty_like(wl.perm)
+        off_i = torch.empty_like(wl.part_off)
+        lar_i = torch.zeros(4, dtype=torch.int64, device=dev)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        for rep in range(11):
+            if rep == 1:
+                ev[0].record()
+            smoe.smoe_predict_shuffle_inter(wl.desc, wl.ids_d, wl.conf_d, wl.emap_d,
+                                            wl.inter["prev"], wl.inter["table"], pred_i, perm_i,
+                                            off_i, wl.ws, x=wl.x, x_shuf=wl.x_shuf)
+        ev[1].record()
+        smoe.smoe_lar(wl.desc, wl.idx, wl.emap_d, lar_i, wl.ws, src_part=pred_i)
+        torch.cuda.synchronize()
+        li = lar_i.cpu().numpy()
+        inter_info = {"alpha_sTS_inter": float(li[0] / li[1]),
+                      "predict_shuffle_inter_ms": round(ev[0].elapsed_time(ev[1]) / 10, 4)}
     result = {
         "metric": "MoE-layer tokens/s (gate+top-K, s-TS predict+shuffle, LAR, dispatch, grouped "
                   "SwiGLU FFN, combine) on GB300",
@@ -511,6 +553,10 @@ def run_native(args):
                   "max": float(lar[3] / lar[1])},
         "wall_s_timed": round(wall, 3),
     }
+    if inter_info is not None:
+        result["alpha"]["sTS_with_table_A"] = inter_info["alpha_sTS_inter"]
+        result["stages"]["predict_shuffle_inter (outside the step)"] = {
+            "ms": inter_info["predict_shuffle_inter_ms"]}
     if wl.prefetch is not None:
         result["prefetch_hit_rate"] = float(wl.prefetch["hits"].item() / (cfg.T * cfg.K))
     if rank == 0:

@@ -126,6 +126,29 @@ SMOE_API int smoe_predict_shuffle(const smoe_desc* desc, const int32_t* token_id
                                   int32_t* pred_part, int32_t* shuf_perm, int32_t* part_off,
                                   void* x_shuf, void* ws, size_t ws_bytes, void* stream);
 
+/* A token's cluster at this layer ("Speculative MoE" §4.1 inter-layer route prediction
+ * models each token's sequence of clusters, i.e. devices, across layers): the partition
+ * holding the most of its K routed experts, the lower partition on ties.
+ *   topk_idx [T, K] int32, expert_part [E] int32, cluster [T] int32 out.             */
+SMOE_API int smoe_token_cluster(const smoe_desc* desc, const int32_t* topk_idx,
+                                const int32_t* expert_part, int32_t* cluster, void* ws,
+                                size_t ws_bytes, void* stream);
+
+/* a3/a4 with both prediction sources of "Speculative MoE" §4.1: the intra-layer C_p
+ * lookup and the inter-layer 2-gram table A over the token's cluster sequence, adopting
+ * the more confident one. Intra confidence = best partition score / K (fp32); inter
+ * confidence = max_p table_a[prev_cluster[t], p]; A's pick (its first maximum) is
+ * adopted only when strictly more confident.
+ *   prev_cluster [T] int32 in [0, P): the token's cluster at the previous layer
+ *   table_a      [P, P] fp32: A[c, p] = Pr(cluster p here | cluster c before)
+ *   other arguments as smoe_predict_shuffle.                                         */
+SMOE_API int smoe_predict_shuffle_inter(const smoe_desc* desc, const int32_t* token_ids,
+                                        const float* conf, const int32_t* expert_part,
+                                        const int32_t* prev_cluster, const float* table_a,
+                                        const void* x, int32_t* pred_part, int32_t* shuf_perm,
+                                        int32_t* part_off, void* x_shuf, void* ws,
+                                        size_t ws_bytes, void* stream);
+
 /* Workspace-free variant of smoe_predict_shuffle, for callers that cannot allocate
  * device memory: code running while a CUDA graph is being captured (where allocation
  * calls are not allowed), runtimes that forbid allocation after start-up, or hosts

@@ -54,6 +54,9 @@ SIGNATURES = {
     "smoe_predict_shuffle": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "smoe_predict_shuffle_noalloc": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "smoe_lar": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _SZ, _P]),
+    "smoe_token_cluster": (ctypes.c_int, [_D, _P, _P, _P, _P, _SZ, _P]),
+    "smoe_predict_shuffle_inter": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                                  _SZ, _P]),
     "smoe_dispatch": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "smoe_expert_ffn": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "smoe_combine": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -157,6 +160,21 @@ def smoe_predict_shuffle_noalloc(desc, token_ids, conf, expert_part, pred_part, 
                                               _ptr(expert_part), _ptr(x), _ptr(pred_part),
                                               _ptr(shuf_perm), _ptr(part_off), _ptr(x_shuf),
                                               _stream(stream)), "smoe_predict_shuffle_noalloc")
+
+
+def smoe_token_cluster(desc, topk_idx, expert_part, cluster, ws, stream=None):
+    _check(lib().smoe_token_cluster(ctypes.byref(desc), _ptr(topk_idx), _ptr(expert_part),
+                                    _ptr(cluster), _ptr(ws), ws.numel(), _stream(stream)),
+           "smoe_token_cluster")
+
+
+def smoe_predict_shuffle_inter(desc, token_ids, conf, expert_part, prev_cluster, table_a,
+                               pred_part, shuf_perm, part_off, ws, x=None, x_shuf=None,
+                               stream=None):
+    _check(lib().smoe_predict_shuffle_inter(
+        ctypes.byref(desc), _ptr(token_ids), _ptr(conf), _ptr(expert_part), _ptr(prev_cluster),
+        _ptr(table_a), _ptr(x), _ptr(pred_part), _ptr(shuf_perm), _ptr(part_off), _ptr(x_shuf),
+        _ptr(ws), ws.numel(), _stream(stream)), "smoe_predict_shuffle_inter")
 
 
 def smoe_lar(desc, topk_idx, expert_part, counts, ws, src_part=None, stream=None):

@@ -235,6 +235,52 @@ SMOE_API int smoe_predict_shuffle(const smoe_desc* desc, const int32_t* token_id
   return SMOE_OK;
 }
 
+SMOE_API int smoe_token_cluster(const smoe_desc* desc, const int32_t* topk_idx,
+                                const int32_t* expert_part, int32_t* cluster, void* ws,
+                                size_t ws_bytes, void* stream) {
+  SMOE_CHECK(check_desc(desc));
+  SMOE_PTR(topk_idx);
+  SMOE_PTR(expert_part);
+  SMOE_PTR(cluster);
+  SMOE_CHECK(check_ws(desc, ws, ws_bytes));
+  SMOE_CHECK(check_device());
+  if (desc->T == 0) return SMOE_OK;
+  cudaError_t e = launch_token_cluster(*desc, topk_idx, expert_part, cluster, ws,
+                                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "token cluster launch");
+  return SMOE_OK;
+}
+
+SMOE_API int smoe_predict_shuffle_inter(const smoe_desc* desc, const int32_t* token_ids,
+                                        const float* conf, const int32_t* expert_part,
+                                        const int32_t* prev_cluster, const float* table_a,
+                                        const void* x, int32_t* pred_part, int32_t* shuf_perm,
+                                        int32_t* part_off, void* x_shuf, void* ws,
+                                        size_t ws_bytes, void* stream) {
+  SMOE_CHECK(check_desc(desc));
+  SMOE_PTR(token_ids);
+  SMOE_PTR(conf);
+  SMOE_PTR(expert_part);
+  SMOE_PTR(prev_cluster);
+  SMOE_PTR(table_a);
+  SMOE_PTR(pred_part);
+  SMOE_PTR(shuf_perm);
+  SMOE_PTR(part_off);
+  SMOE_OPT_PTR(x_shuf);
+  if (x_shuf) SMOE_PTR(x);
+  SMOE_CHECK(check_ws(desc, ws, ws_bytes));
+  SMOE_CHECK(check_device());
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (desc->T == 0) {
+    SMOE_CUDA(cudaMemsetAsync(part_off, 0, sizeof(int32_t) * (desc->P + 1), s));
+    return SMOE_OK;
+  }
+  cudaError_t e = launch_predict_shuffle(*desc, token_ids, conf, expert_part, x, pred_part,
+                                         shuf_perm, part_off, x_shuf, ws, s, prev_cluster, table_a);
+  if (e != cudaSuccess) return cuda_fail(e, "predict/shuffle launch");
+  return SMOE_OK;
+}
+
 SMOE_API int smoe_lar(const smoe_desc* desc, const int32_t* topk_idx, const int32_t* src_part,
                       const int32_t* expert_part, unsigned long long* counts, void* ws,
                       size_t ws_bytes, void* stream) {

@@ -171,10 +171,15 @@ cudaError_t launch_route(const smoe_desc& d, int rows, const void* x, const void
                          float* topk_w, void* ws, cudaStream_t s,
                          RouteSplitOut so = RouteSplitOut{0x7fffffff, nullptr, nullptr, nullptr});
 
+// prev_cluster / table_a non-NULL: the inter-layer source also votes (see sort.cu).
 cudaError_t launch_predict_shuffle(const smoe_desc& d, const int32_t* ids, const float* conf,
                                    const int32_t* emap, const void* x, int32_t* pred,
                                    int32_t* perm, int32_t* part_off, void* x_shuf, void* ws,
-                                   cudaStream_t s);
+                                   cudaStream_t s, const int32_t* prev_cluster = nullptr,
+                                   const float* table_a = nullptr);
+
+cudaError_t launch_token_cluster(const smoe_desc& d, const int32_t* idx, const int32_t* emap,
+                                 int32_t* cluster, void* ws, cudaStream_t s);
 
 cudaError_t launch_lar(const smoe_desc& d, const int32_t* idx, const int32_t* src_part,
                        const int32_t* emap, unsigned long long* counts, void* ws,

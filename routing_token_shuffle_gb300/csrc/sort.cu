@@ -37,11 +37,17 @@ __device__ __forceinline__ unsigned lanemask_lt() {
 // launcher zeroes first).
 constexpr int kPredTokens = 64;
 
+// INTER: the inter-layer source of "Speculative MoE" §4.1 also votes. prev[t] is the
+// token's cluster at the previous layer and table_a [P, P] the 2-gram table A; A's row
+// maximum (first maximum) replaces the intra-layer pick when it is strictly larger than
+// the intra-layer confidence (best partition score / K, an IEEE fp32 division).
+template <bool INTER>
 __global__ void __launch_bounds__(kThreads)
 predict_hist_kernel(const int32_t* __restrict__ ids, const float* __restrict__ conf,
                     const int32_t* __restrict__ emap, int T, int E, int P, int vocab,
                     int32_t* __restrict__ pred, int32_t* __restrict__ hist, int ntiles,
-                    DeviceStatus* st) {
+                    DeviceStatus* st, const int32_t* __restrict__ prev,
+                    const float* __restrict__ table_a, int K) {
   pdl_wait_and_trigger();
   extern __shared__ float s_rows[];          // [kPredTokens, E]
   __shared__ int s_map[kMaxBuckets];
@@ -120,7 +126,24 @@ predict_hist_kernel(const int32_t* __restrict__ ids, const float* __restrict__ c
       if (os > sc || (os == sc && oi < bi)) { sc = os; bi = oi; }
     }
     // an invalid id, or a NaN/inf row (outside the contract), gives partition 0
-    const int best = (s_id[i] >= 0 && (unsigned)bi < (unsigned)P) ? bi : 0;
+    int best = (s_id[i] >= 0 && (unsigned)bi < (unsigned)P) ? bi : 0;
+    if (INTER && s_id[i] >= 0) {
+      int c = prev[t0 + i];
+      if ((unsigned)c >= (unsigned)P) {
+        if (lane == 0) record_error(st, kStatusData, kBadSrcPart, t0 + i);
+        c = 0;
+      }
+      float av = lane < P ? table_a[c * P + lane] : -INFINITY;
+      int ai = lane;
+#pragma unroll
+      for (int off = 16; off; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, av, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, ai, off);
+        if (ov > av || (ov == av && oi < ai)) { av = ov; ai = oi; }
+      }
+      const float conf_intra = sc / (float)K;
+      if (av > conf_intra && (unsigned)ai < (unsigned)P) best = ai;
+    }
     if (lane == 0) {
       pred[t0 + i] = best;
       atomicAdd(&s_cnt[best], 1);
@@ -301,6 +324,41 @@ gather_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
   }
 }
 
+// ------------------------------------------------------------------ token cluster
+// cluster[t] = the partition holding the most of token t's experts, the lower partition
+// on ties (a token's cluster, or device, at this layer).
+__global__ void __launch_bounds__(kThreads)
+token_cluster_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ emap, int T,
+                     int K, int E, int P, int32_t* __restrict__ cluster, DeviceStatus* st) {
+  pdl_wait_and_trigger();
+  const int t = blockIdx.x * kThreads + threadIdx.x;
+  if (t >= T) return;
+  const int32_t* row = idx + (size_t)t * K;
+  int best_p = 0, best_c = -1;
+  for (int k = 0; k < K; ++k) {
+    const int e = row[k];
+    if ((unsigned)e >= (unsigned)E) {
+      record_error(st, kStatusData, kBadTopkIdx, (long long)t * K + k);
+      continue;
+    }
+    const int p = emap[e];
+    if ((unsigned)p >= (unsigned)P) {
+      record_error(st, kStatusData, kBadExpertPart, e);
+      continue;
+    }
+    int c = 0;
+    for (int k2 = 0; k2 < K; ++k2) {
+      const int e2 = row[k2];
+      c += ((unsigned)e2 < (unsigned)E && emap[e2] == p);
+    }
+    if (c > best_c || (c == best_c && p < best_p)) {
+      best_c = c;
+      best_p = p;
+    }
+  }
+  cluster[t] = best_p;
+}
+
 // ------------------------------------------------------------------ LAR
 __device__ __forceinline__ int foe_source(int t, int h, int G, int H) {
   return H >= G ? (h * G) / H : h * (G / H) + (t % (G / H));
@@ -390,7 +448,8 @@ int grid_for_rows(long long nrows) {
 cudaError_t launch_predict_shuffle(const smoe_desc& d, const int32_t* ids, const float* conf,
                                    const int32_t* emap, const void* x, int32_t* pred,
                                    int32_t* perm, int32_t* part_off, void* x_shuf, void* ws,
-                                   cudaStream_t s) {
+                                   cudaStream_t s, const int32_t* prev_cluster,
+                                   const float* table_a) {
   WsLayout L;
   ws_layout(d, &L);
   DeviceStatus* st = ws_ptr<DeviceStatus>(ws, L.status);
@@ -399,11 +458,20 @@ cudaError_t launch_predict_shuffle(const smoe_desc& d, const int32_t* ids, const
   const int ntiles = ceil_div(d.T, kSortTile);
   cudaError_t e = cudaMemsetAsync(hist, 0, sizeof(int32_t) * d.P * ntiles, s);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(predict_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(predict_hist_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)predict_smem(d.E));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(predict_hist_kernel<true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)predict_smem(d.E));
   if (e != cudaSuccess) return e;
-  SMOE_LAUNCH(predict_hist_kernel, ceil_div(d.T, kPredTokens), kThreads, predict_smem(d.E), s, ids,
-      conf, emap, d.T, d.E, d.P, d.vocab, pred, hist, ntiles, st);
+  if (prev_cluster)
+    SMOE_LAUNCH(predict_hist_kernel<true>, ceil_div(d.T, kPredTokens), kThreads, predict_smem(d.E),
+        s, ids, conf, emap, d.T, d.E, d.P, d.vocab, pred, hist, ntiles, st, prev_cluster,
+        table_a, d.K);
+  else
+    SMOE_LAUNCH(predict_hist_kernel<false>, ceil_div(d.T, kPredTokens), kThreads,
+        predict_smem(d.E), s, ids, conf, emap, d.T, d.E, d.P, d.vocab, pred, hist, ntiles, st,
+        nullptr, nullptr, d.K);
   SMOE_LAUNCH(scan_kernel, 1, 1024, 0, s, hist, offs, d.P * ntiles, d.P, ntiles, d.T, part_off);
   SMOE_LAUNCH(scatter_kernel<kShuffle>, ntiles, kThreads, 0, s, pred, d.T, d.P, ntiles, offs, perm,
       nullptr, 0, 0, nullptr, nullptr, nullptr);
@@ -440,6 +508,15 @@ cudaError_t launch_dispatch(const smoe_desc& d, const int32_t* idx, const int32_
     SMOE_LAUNCH(gather_rows_kernel, grid_for_rows(n), kThreads, 0, s,
         static_cast<const uint4*>(x_src), static_cast<uint4*>(x_disp), row_src, n, d.T, vec, st);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_token_cluster(const smoe_desc& d, const int32_t* idx, const int32_t* emap,
+                                 int32_t* cluster, void* ws, cudaStream_t s) {
+  WsLayout L;
+  ws_layout(d, &L);
+  SMOE_LAUNCH(token_cluster_kernel, ceil_div(d.T, kThreads), kThreads, 0, s, idx, emap, d.T, d.K,
+              d.E, d.P, cluster, ws_ptr<DeviceStatus>(ws, L.status));
   return cudaGetLastError();
 }
 
@@ -539,11 +616,12 @@ extern "C" SMOE_API int smoe_predict_shuffle_noalloc(const smoe_desc* desc,
   const smoe_desc& d = *desc;
   cudaError_t ce = cudaMemsetAsync(hist, 0, sizeof(int32_t) * d.P * ntiles, s);
   if (ce == cudaSuccess)
-    ce = cudaFuncSetAttribute(predict_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)predict_smem(d.E));
+    ce = cudaFuncSetAttribute(predict_hist_kernel<false>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)predict_smem(d.E));
   if (ce != cudaSuccess) return set_last_error(SMOE_ERR_CUDA, cudaGetErrorString(ce));
-  SMOE_LAUNCH_STATUS(predict_hist_kernel, ceil_div(d.T, kPredTokens), kThreads, predict_smem(d.E),
-      s, token_ids, conf, expert_part, d.T, d.E, d.P, d.vocab, pred_part, hist, ntiles, nullptr);
+  SMOE_LAUNCH_STATUS(predict_hist_kernel<false>, ceil_div(d.T, kPredTokens), kThreads,
+      predict_smem(d.E), s, token_ids, conf, expert_part, d.T, d.E, d.P, d.vocab, pred_part, hist,
+      ntiles, nullptr, nullptr, nullptr, d.K);
   SMOE_LAUNCH_STATUS(scan_kernel, 1, 1024, 0, s, hist, offs, d.P * ntiles, d.P, ntiles, d.T,
       part_off);
   SMOE_LAUNCH_STATUS(scatter_kernel<kShuffle>, ntiles, kThreads, 0, s, pred_part, d.T, d.P, ntiles,

@@ -63,3 +63,25 @@ def coclustered_placement(profile_idx, E: int, P: int, order) -> np.ndarray:
         place[e] = best
         members[best].append(int(e))
     return place
+
+
+def cluster_of(routes, expert_part, P: int) -> np.ndarray:
+    """Each token's cluster: the partition holding most of its routed experts (lower
+    partition on ties)."""
+    part = np.asarray(expert_part, dtype=np.int64)[np.asarray(routes, dtype=np.int64)]
+    hist = np.zeros((part.shape[0], P), dtype=np.int64)
+    for k in range(part.shape[1]):
+        np.add.at(hist, (np.arange(part.shape[0]), part[:, k]), 1)
+    return hist.argmax(axis=1).astype(np.int32)
+
+
+def transition_table(prev_cluster, cur_cluster, P: int) -> np.ndarray:
+    """Table A [P, P] float32 of "Speculative MoE" §4.1's 2-gram model: the share of the
+    profile tokens of previous cluster c that land in cluster p (uniform if c is unseen)."""
+    idx = np.asarray(prev_cluster, dtype=np.int64) * P + np.asarray(cur_cluster, dtype=np.int64)
+    counts = np.bincount(idx, minlength=P * P).reshape(P, P).astype(np.float64)
+    tot = counts.sum(axis=1, keepdims=True)
+    table = np.full((P, P), 1.0 / P)
+    seen = tot[:, 0] > 0
+    table[seen] = counts[seen] / tot[seen]
+    return table.astype(np.float32)

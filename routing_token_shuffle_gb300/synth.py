@@ -39,7 +39,7 @@ import numpy as np
 import torch
 
 # Stream names spawned from SeedSequence(workload index), in this fixed order.
-STREAMS = ("ids", "emb", "noise", "weights", "profile", "placement", "predictor")
+STREAMS = ("ids", "emb", "noise", "weights", "profile", "placement", "predictor", "prev_layer")
 
 
 @dataclasses.dataclass(frozen=True)
@@ -282,3 +282,12 @@ def predictor_inputs(cfg: LayerConfig, device):
 def profile_batch_for_default_vector(cfg: LayerConfig, emb: Embedding, device, n: int = 1024):
     """The separate seeded token batch whose mean layer output is the default vector d_l."""
     return token_batch(cfg, emb, "predictor", n, device, salt=7)
+
+
+def previous_layer_gate(cfg: LayerConfig, device):
+    """Router weight of a stand-in previous MoE layer [E, d] ~ N(0, 1/d) in the workload
+    dtype: routing the same token representations through it gives each token a
+    previous-layer cluster for the inter-layer predictor."""
+    g = _torch_gen(_streams(cfg.seed_index)["prev_layer"], 0, device)
+    w = torch.randn(cfg.E, cfg.d, generator=g, device=device) / math.sqrt(cfg.d)
+    return w.to(cfg.torch_dtype)

@@ -434,3 +434,42 @@ def test_expert_ffn_two_sm_tiles_ragged(T, E, K, S, d, F):
     assert rel_err_rows(to_np(yd), ref).max() <= VALUE_TOL
     for j in range(S):
         assert rel_err_rows(to_np(ysh[j]), O.swiglu_ffn(xn, *W[E + j])).max() <= VALUE_TOL
+
+
+@pytest.mark.parametrize("name,T", [("tiny_fp32", None), ("dsv2_prefill", 1537), ("qwen3_foe", 3001),
+                                    ("dsv2_prefill", None)],
+                         ids=["tiny", "dsv2-T1537", "qwen3-T3001", "dsv2-full"])
+def test_inter_layer_predictor(name, T):
+    """Token clusters from a previous layer's routes and the more-confident-of-C_p-and-A
+    prediction, bit-exact against the oracle, with table A profiled by the oracle."""
+    c = get_case(name, T)
+    cfg = c.cfg
+    desc = smoe.desc_from_config(cfg)
+    ws = smoe.workspace(desc)
+    wprev = synth.previous_layer_gate(cfg, "cuda")
+    # previous layer's routes of the measured batch (GPU) and cluster per token
+    lg, idx, w = f32(cfg.T, cfg.E), i32(cfg.T, cfg.K), f32(cfg.T, cfg.K)
+    smoe.smoe_route(desc, c.x, wprev, idx, w, logits_out=lg, ws=ws)
+    clus = i32(cfg.T)
+    smoe.smoe_token_cluster(desc, idx, c.emap_d, clus, ws)
+    smoe.smoe_get_status(ws)
+    prev = O.token_cluster(O.topk_select(to_np(lg), cfg.K, cfg.H), c.emap, cfg.P)
+    assert np.array_equal(to_np(clus), prev)
+    # table A from the profile batch, both layers routed by the oracle
+    _, px = synth.token_batch(cfg, c.emb, "profile", min(cfg.profile_tokens, 8192), "cuda")
+    pxn = to_np(px.to(cfg.torch_dtype))
+    _, pidx_prev, _ = O.route(pxn, to_np(wprev), cfg.K, cfg.H)
+    table = O.markov_table(O.token_cluster(pidx_prev, c.emap, cfg.P),
+                           O.token_cluster(c.profile_idx, c.emap, cfg.P), cfg.P)
+    for tab in (table, np.full((cfg.P, cfg.P), 0.9, np.float32) * np.eye(cfg.P, dtype=np.float32)):
+        pred, perm, off = i32(cfg.T), i32(cfg.T), i32(cfg.P + 1)
+        xs = torch.empty_like(c.x)
+        smoe.smoe_predict_shuffle_inter(desc, c.ids_d, c.conf_d, c.emap_d, clus,
+                                        torch.as_tensor(tab, device="cuda"), pred, perm, off, ws,
+                                        x=c.x, x_shuf=xs)
+        smoe.smoe_get_status(ws)
+        ref = O.predict_partition_inter(c.ids, c.conf, c.emap, cfg.P, cfg.K, prev, tab)
+        assert np.array_equal(to_np(pred), ref)
+        rp, ro = O.token_shuffle(ref, cfg.P)
+        assert np.array_equal(to_np(perm), rp) and np.array_equal(to_np(off), ro)
+        assert torch.equal(xs, c.x[torch.as_tensor(rp, device="cuda").long()])
