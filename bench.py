@@ -44,6 +44,8 @@ def parse_args(argv=None):
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--impl", default="native", choices=["native", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-placement", action="store_true",
+                   help="skip the (untimed) co-clustered placement report")
     p.add_argument("--cpu-seconds", type=float, default=15.0,
                    help="target CPU time of the oracle baseline sample")
     return p.parse_args(argv)
@@ -234,6 +236,7 @@ class Workload:
             self.profile_idx = pidx.cpu().numpy()
             del pw, pws
         del px
+        self.profile_ids = pids
         self.conf = profiling.confidence_table(
             pids, self.profile_idx, cfg.vocab, cfg.E, cfg.K,
             emb_rows=lambda v: self.emb.rows(v).cpu().numpy(), rows_needed=self.ids)
@@ -326,6 +329,70 @@ class Workload:
             s.smoe_prefetch_predict(c.desc, p["r"], p["d_l"], c.y, p["gamma"], p["beta"], p["wgn"],
                                     p["pi"], p["ti"], p["hits"], c.ws)
         rec(6)
+
+
+def speculative_execution_report(wl):
+    """Run the next layer's stand-in (this layer's experts) on s = LN(r + y) with the
+    routes predicted from q and with the true routes; report the hit rate, the relative
+    deviation of the speculative output and the time of one routed forward."""
+    import torch
+    s, c, p = wl.smoe, wl.cfg, wl.prefetch
+    dev = wl.dev
+    lq = torch.empty(c.T, c.E, device=dev)
+    ls = torch.empty(c.T, c.E, device=dev)
+    qs = torch.empty(2, c.T, c.d, dtype=c.torch_dtype, device=dev)
+    s.smoe_prefetch_predict(wl.desc, p["r"], p["d_l"], wl.y, p["gamma"], p["beta"], p["wgn"],
+                            p["pi"], p["ti"], p["hits"], wl.ws, logits_q=lq, logits_s=ls,
+                            qs_out=qs)
+    i32 = dict(dtype=torch.int32, device=dev)
+    pidx, tidx = torch.empty(c.T, c.K, **i32), torch.empty(c.T, c.K, **i32)
+    pw, tw = torch.empty(c.T, c.K, device=dev), torch.empty(c.T, c.K, device=dev)
+    s.smoe_route(wl.desc, None, None, pidx, pw, logits_in=lq)
+    s.smoe_route(wl.desc, None, None, tidx, tw, logits_in=ls)
+    s_rows = qs[1].contiguous()
+    y_spec, y_true = torch.empty_like(wl.x), torch.empty_like(wl.x)
+    s.smoe_moe_forward_routed(wl.desc, s_rows, tidx, tw, wl.w1, wl.w3, wl.w2, y_true, wl.ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(5):
+        s.smoe_moe_forward_routed(wl.desc, s_rows, pidx, pw, wl.w1, wl.w3, wl.w2, y_spec, wl.ws)
+    e1.record()
+    torch.cuda.synchronize()
+    d = (y_spec.float() - y_true.float()).norm() / y_true.float().norm()
+    return {"hit_rate": float(p["hits"].item() / (c.T * c.K)),
+            "rel_deviation_fro": round(float(d), 4),
+            "routed_forward_ms": round(e0.elapsed_time(e1) / 5, 4)}
+
+
+def placement_report(wl):
+    """Offline s-EG placement: co-cluster the profile batch's token-expert activations
+    (cross-entropy optimisation, seeded) and measure, on this batch, α and the imbalance
+    of the predicted partitions (largest / mean) under the workload's map and under the
+    co-clustered map. Not timed; the layer step keeps the workload's map."""
+    import time
+
+    import numpy as np
+    import torch
+    from routing_token_shuffle_gb300 import profiling
+    s, c = wl.smoe, wl.cfg
+    t0 = time.perf_counter()
+    act = profiling.activation_counts(wl.profile_ids, wl.profile_idx, c.vocab, c.E)
+    m, _, cost = profiling.ceo_placement(act, c.P, theta=0.1, seed=0)
+    secs = time.perf_counter() - t0
+    out = {"tool_s": round(secs, 2), "objective_theta_0.1": round(cost, 4)}
+    for name, emap in (("workload_map", wl.emap), ("coclustered_map", m)):
+        em = torch.as_tensor(np.ascontiguousarray(emap, dtype=np.int32), device=wl.dev)
+        pred, perm = torch.empty_like(wl.pred), torch.empty_like(wl.perm)
+        off = torch.empty_like(wl.part_off)
+        lar = torch.zeros(4, dtype=torch.int64, device=wl.dev)
+        s.smoe_predict_shuffle(wl.desc, wl.ids_d, wl.conf_d, em, pred, perm, off, wl.ws)
+        s.smoe_lar(wl.desc, wl.idx, em, lar, wl.ws, src_part=pred)
+        torch.cuda.synchronize()
+        li, sizes = lar.cpu().numpy(), np.diff(off.cpu().numpy())
+        out[name] = {"alpha_sTS": round(float(li[0] / li[1]), 4),
+                     "alpha_base": round(float(li[2] / li[1]), 4),
+                     "partition_imbalance": round(float(sizes.max() / sizes.mean()), 3)}
+    return out
 
 
 # ----------------------------------------------------------------- CPU oracle
@@ -557,8 +624,11 @@ def run_native(args):
         result["alpha"]["sTS_with_table_A"] = inter_info["alpha_sTS_inter"]
         result["stages"]["predict_shuffle_inter (outside the step)"] = {
             "ms": inter_info["predict_shuffle_inter_ms"]}
+    if not args.no_placement:
+        result["placement"] = placement_report(wl)
     if wl.prefetch is not None:
         result["prefetch_hit_rate"] = float(wl.prefetch["hits"].item() / (cfg.T * cfg.K))
+        result["speculative_execution"] = speculative_execution_report(wl)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if active:

@@ -281,13 +281,25 @@ SMOE_API int smoe_layer_forward_host(const smoe_desc* desc, const smoe_layer_wei
  *   r [T, d] fp32 residual; d_l [d] fp32 default vector; y [T, d] dtype layer output;
  *   gamma, beta [d] fp32 (LayerNorm over d, biased variance, eps 1e-5);
  *   w_gate_next [E, d] dtype; logits_q, logits_s nullable [T, E] fp32;
- *   pred_idx, true_idx [T, K] int32; hits [1] uint64, overwritten.                  */
+ *   pred_idx, true_idx [T, K] int32; hits [1] uint64, overwritten;
+ *   qs_out nullable [2, T, d] dtype: the q rows then the s rows (else kept in ws).     */
 SMOE_API int smoe_prefetch_predict(const smoe_desc* desc, const float* r, const float* d_l,
                                    const void* y, const float* gamma, const float* beta,
                                    const void* w_gate_next, float* logits_q, float* logits_s,
                                    int32_t* pred_idx, int32_t* true_idx,
-                                   unsigned long long* hits, void* ws, size_t ws_bytes,
-                                   void* stream);
+                                   unsigned long long* hits, void* qs_out, void* ws,
+                                   size_t ws_bytes, void* stream);
+
+/* The MoE body with routes supplied by the caller: dispatch (token order, no shuffle),
+ * grouped SwiGLU FFN (shared experts included) and combine. With the routes predicted
+ * by smoe_prefetch_predict this is speculative execution ("Speculating Experts ..."
+ * §2.B: the predicted experts run instead of the router's true ones).
+ *   x [T, d] dtype; topk_idx [T, K] int32 in [0, E); topk_w [T, K] fp32;
+ *   w1, w3, w2 as smoe_expert_ffn; y [T, d] dtype out.                                */
+SMOE_API int smoe_moe_forward_routed(const smoe_desc* desc, const void* x,
+                                     const int32_t* topk_idx, const float* topk_w,
+                                     const void* w1, const void* w3, const void* w2, void* y,
+                                     void* ws, size_t ws_bytes, void* stream);
 
 /* Synchronises `stream`, returns SMOE_OK, SMOE_ERR_DATA or SMOE_ERR_DEVICE_TIMEOUT from
  * the workspace status word, and clears it. */

@@ -422,6 +422,16 @@ def prefetch_predict(r, d_l, y, gamma, beta, w_gate_next, K, H=1, eps=1e-5,
                 true_idx=true_idx, hits=hit_count(pred_idx, true_idx))
 
 
+def speculative_execution(s_rows, pred_idx, pred_w, true_idx, true_w, w1, w3, w2, n_shared=0):
+    """[SpecE §2.B] Run the experts predicted from q (weights from q's logits) instead of
+    the router's true ones on the same next-layer input s. Returns the speculative output,
+    the true output and the relative Frobenius deviation between them."""
+    y_spec = moe_output(s_rows, pred_idx, pred_w, w1, w3, w2, n_shared)
+    y_true = moe_output(s_rows, true_idx, true_w, w1, w3, w2, n_shared)
+    dev = float(np.linalg.norm(y_spec - y_true) / max(np.linalg.norm(y_true), 1e-300))
+    return y_spec, y_true, dev
+
+
 # ----------------------------------------------------------------------------
 # Offline tables                                             [sMoE §4.1, Fig. 3]
 # ----------------------------------------------------------------------------
@@ -457,6 +467,41 @@ def profile_confidence(profile_ids, profile_idx, vocab, E, K, emb_rows=None, row
                 nn = np.argmax(eu @ es.T, axis=1)     # first maximum: lower seen id
                 conf[blk] = conf[seen[nn]]
     return conf.astype(np.float32)
+
+
+def coclustering_cost(act, expert_part, token_part, P, theta):
+    """Objective of balanced token-expert co-clustering [sMoE §4.2]: theta times the load
+    imbalance (token frequency per cluster: (max - mean) / mean) plus (1 - theta) times the
+    remote activations (share of token-expert activations whose token and expert sit in
+    different clusters). act [V, E]: activation counts of each token id and expert."""
+    act = np.asarray(act, dtype=np.float64)
+    m = np.asarray(expert_part, dtype=np.int64)
+    tau = np.asarray(token_part, dtype=np.int64)
+    freq = act.sum(axis=1)
+    load = np.array([freq[tau == p].sum() for p in range(P)])
+    mean = load.mean()
+    imbalance = (load.max() - mean) / mean if mean > 0 else 0.0
+    remote = sum(act[v, e] for v in range(act.shape[0]) for e in range(act.shape[1])
+                 if m[e] != tau[v])
+    total = act.sum()
+    return theta * imbalance + (1.0 - theta) * (remote / total if total > 0 else 0.0)
+
+
+def coclustering_bruteforce(act, P, theta):
+    """Exact optimum of coclustering_cost over every balanced expert map (E/P experts per
+    cluster) and every token map, for tiny instances. Returns (cost, expert_part, token_part)."""
+    import itertools
+    act = np.asarray(act, dtype=np.float64)
+    V, E = act.shape
+    best = (np.inf, None, None)
+    for m in itertools.product(range(P), repeat=E):
+        if any(m.count(p) != E // P for p in range(P)):
+            continue
+        for tau in itertools.product(range(P), repeat=V):
+            c = coclustering_cost(act, m, tau, P, theta)
+            if c < best[0] - 1e-15:
+                best = (c, np.array(m, np.int32), np.array(tau, np.int32))
+    return best
 
 
 # ----------------------------------------------------------------------------

@@ -65,7 +65,8 @@ SIGNATURES = {
     "smoe_layer_forward_host": (ctypes.c_int, [_D, ctypes.POINTER(LayerWeights), _P, _P, _P, _P,
                                                _SZ, _P]),
     "smoe_prefetch_predict": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
-                                             _SZ, _P]),
+                                             _P, _SZ, _P]),
+    "smoe_moe_forward_routed": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "smoe_get_status": (ctypes.c_int, [_P, _P]),
     "smoe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "smoe_last_error": (ctypes.c_char_p, []),
@@ -231,12 +232,19 @@ def smoe_layer_forward_host(desc, weights: LayerWeights, x_host, ids_host, y_hos
 
 
 def smoe_prefetch_predict(desc, r, d_l, y, gamma, beta, w_gate_next, pred_idx, true_idx, hits, ws,
-                          logits_q=None, logits_s=None, stream=None):
+                          logits_q=None, logits_s=None, qs_out=None, stream=None):
     _check(lib().smoe_prefetch_predict(ctypes.byref(desc), _ptr(r), _ptr(d_l), _ptr(y), _ptr(gamma),
                                        _ptr(beta), _ptr(w_gate_next), _ptr(logits_q),
                                        _ptr(logits_s), _ptr(pred_idx), _ptr(true_idx), _ptr(hits),
-                                       _ptr(ws), ws.numel(), _stream(stream)),
+                                       _ptr(qs_out), _ptr(ws), ws.numel(), _stream(stream)),
            "smoe_prefetch_predict")
+
+
+def smoe_moe_forward_routed(desc, x, topk_idx, topk_w, w1, w3, w2, y, ws, stream=None):
+    _check(lib().smoe_moe_forward_routed(ctypes.byref(desc), _ptr(x), _ptr(topk_idx),
+                                         _ptr(topk_w), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(y),
+                                         _ptr(ws), ws.numel(), _stream(stream)),
+           "smoe_moe_forward_routed")
 
 
 def kernel_launches() -> int:

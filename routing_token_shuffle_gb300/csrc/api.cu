@@ -475,12 +475,45 @@ SMOE_API int smoe_layer_forward_host(const smoe_desc* desc, const smoe_layer_wei
   return SMOE_OK;
 }
 
+SMOE_API int smoe_moe_forward_routed(const smoe_desc* desc, const void* x,
+                                     const int32_t* topk_idx, const float* topk_w,
+                                     const void* w1, const void* w3, const void* w2, void* y,
+                                     void* ws, size_t ws_bytes, void* stream) {
+  SMOE_CHECK(check_desc(desc));
+  SMOE_PTR(x);
+  SMOE_PTR(topk_idx);
+  SMOE_PTR(topk_w);
+  SMOE_PTR(w1);
+  SMOE_PTR(w3);
+  SMOE_PTR(w2);
+  SMOE_PTR(y);
+  SMOE_CHECK(check_ws(desc, ws, ws_bytes));
+  SMOE_CHECK(check_device());
+  if (desc->T == 0) return SMOE_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  WsLayout L;
+  ws_layout(*desc, &L);
+  int32_t* expert_off = ws_ptr<int32_t>(ws, L.expert_off);
+  int32_t* pair_row = ws_ptr<int32_t>(ws, L.pair_row);
+  int32_t* row_token = ws_ptr<int32_t>(ws, L.row_token);
+  void* x_disp = ws_ptr<char>(ws, L.x_disp);
+  void* y_sh = desc->n_shared ? ws_ptr<char>(ws, L.y_sh) : nullptr;
+  cudaError_t e = launch_dispatch(*desc, topk_idx, nullptr, x, expert_off, pair_row, row_token,
+                                  nullptr, x_disp, ws, s);
+  if (e != cudaSuccess) return cuda_fail(e, "dispatch launch");
+  e = launch_expert_ffn(*desc, x_disp, x, expert_off, w1, w3, w2, x_disp, y_sh, ws, s);
+  if (e != cudaSuccess) return cuda_fail(e, "expert ffn launch");
+  e = launch_combine(*desc, x_disp, pair_row, topk_w, y_sh, y, ws, s);
+  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  return SMOE_OK;
+}
+
 SMOE_API int smoe_prefetch_predict(const smoe_desc* desc, const float* r, const float* d_l,
                                    const void* y, const float* gamma, const float* beta,
                                    const void* w_gate_next, float* logits_q, float* logits_s,
                                    int32_t* pred_idx, int32_t* true_idx,
-                                   unsigned long long* hits, void* ws, size_t ws_bytes,
-                                   void* stream) {
+                                   unsigned long long* hits, void* qs_out, void* ws,
+                                   size_t ws_bytes, void* stream) {
   SMOE_CHECK(check_desc(desc));
   SMOE_REQUIRE(desc->d <= 8192, SMOE_ERR_SHAPE, "prefetch predictor supports d <= 8192");
   SMOE_PTR(r);
@@ -494,6 +527,7 @@ SMOE_API int smoe_prefetch_predict(const smoe_desc* desc, const float* r, const 
   SMOE_PTR(hits);
   SMOE_OPT_PTR(logits_q);
   SMOE_OPT_PTR(logits_s);
+  SMOE_OPT_PTR(qs_out);
   SMOE_CHECK(check_ws(desc, ws, ws_bytes));
   SMOE_CHECK(check_device());
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -503,7 +537,7 @@ SMOE_API int smoe_prefetch_predict(const smoe_desc* desc, const float* r, const 
   }
   WsLayout L;
   ws_layout(*desc, &L);
-  char* qs = ws_ptr<char>(ws, L.pf_qs);
+  char* qs = qs_out ? static_cast<char*>(qs_out) : ws_ptr<char>(ws, L.pf_qs);
   float* lg = ws_ptr<float>(ws, L.pf_logits);
   float* wq = ws_ptr<float>(ws, L.pf_idx);
   const size_t T = desc->T;

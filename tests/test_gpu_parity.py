@@ -473,3 +473,71 @@ def test_inter_layer_predictor(name, T):
         rp, ro = O.token_shuffle(ref, cfg.P)
         assert np.array_equal(to_np(perm), rp) and np.array_equal(to_np(off), ro)
         assert torch.equal(xs, c.x[torch.as_tensor(rp, device="cuda").long()])
+
+
+@pytest.mark.parametrize("name,T", [("dsv2_prefill", 1537), ("mixtral", 1001)], ids=["dsv2", "mixtral"])
+def test_moe_forward_routed(name, T):
+    """The MoE body with caller-supplied routes, against the oracle's defining sum."""
+    c = get_case(name, T)
+    cfg = c.cfg
+    desc = smoe.desc_from_config(cfg)
+    ws = smoe.workspace(desc)
+    rng = np.random.default_rng(41)
+    L = (rng.standard_normal((cfg.T, cfg.E)) * 2).astype(np.float32)
+    idx = O.topk_select(L, cfg.K, cfg.H)
+    w = O.gate_weights(L, idx).astype(np.float32)
+    y = torch.empty_like(c.x)
+    smoe.smoe_moe_forward_routed(desc, c.x, torch.as_tensor(idx, device="cuda"),
+                                 torch.as_tensor(w, device="cuda"), c.w1, c.w3, c.w2, y, ws)
+    smoe.smoe_get_status(ws)
+    toks = sample_tokens(cfg.T, 24, seed=6)
+    ref = c.oracle_tokens(toks, idx, w.astype(np.float64))
+    assert rel_err_rows(to_np(y)[toks], ref).max() <= VALUE_TOL
+
+
+def test_speculative_execution_qwen3():
+    """Prefetch predictor -> speculative execution of the predicted experts on the next
+    layer's input s, against the oracle on the same s rows and logits."""
+    c = get_case("qwen3_foe", 3001)
+    cfg = c.cfg
+    desc = smoe.desc_from_config(cfg)
+    ws = smoe.workspace(desc)
+    r, wgn, gamma, beta = synth.predictor_inputs(cfg, "cuda")
+    wgn_l = wgn.to(cfg.torch_dtype)
+    d_l = synth.round_bf16(torch.randn(cfg.d, device="cuda", generator=torch.Generator(
+        device="cuda").manual_seed(12)) * 0.3)
+    W = smoe.layer_weights(c.w_gate, c.w1, c.w3, c.w2, c.conf_d, c.emap_d)
+    y = torch.empty_like(c.x)
+    smoe.smoe_layer_forward(desc, W, smoe.layer_io(c.x, c.ids_d, y), ws)
+    lq, ls = f32(cfg.T, cfg.E), f32(cfg.T, cfg.E)
+    pi, ti = i32(cfg.T, cfg.K), i32(cfg.T, cfg.K)
+    hits = torch.empty(1, dtype=torch.int64, device="cuda")
+    qs = torch.empty(2, cfg.T, cfg.d, dtype=cfg.torch_dtype, device="cuda")
+    smoe.smoe_prefetch_predict(desc, r, d_l, y, gamma, beta, wgn_l, pi, ti, hits, ws,
+                               logits_q=lq, logits_s=ls, qs_out=qs)
+    pidx, pw, tidx, tw = i32(cfg.T, cfg.K), f32(cfg.T, cfg.K), i32(cfg.T, cfg.K), f32(cfg.T, cfg.K)
+    smoe.smoe_route(desc, None, None, pidx, pw, logits_in=lq)
+    smoe.smoe_route(desc, None, None, tidx, tw, logits_in=ls)
+    assert torch.equal(pidx, pi) and torch.equal(tidx, ti)
+    s_rows = qs[1].contiguous()
+    y_spec, y_true = torch.empty_like(c.x), torch.empty_like(c.x)
+    smoe.smoe_moe_forward_routed(desc, s_rows, pidx, pw, c.w1, c.w3, c.w2, y_spec, ws)
+    smoe.smoe_moe_forward_routed(desc, s_rows, tidx, tw, c.w1, c.w3, c.w2, y_true, ws)
+    smoe.smoe_get_status(ws)
+    torch.cuda.synchronize()
+    toks = sample_tokens(cfg.T, 24, seed=7)
+    Lq, Ls = to_np(lq), to_np(ls)
+    p_idx, t_idx = O.topk_select(Lq, cfg.K, cfg.H), O.topk_select(Ls, cfg.K, cfg.H)
+    p_w, t_w = O.gate_weights(Lq, p_idx), O.gate_weights(Ls, t_idx)
+    sn = to_np(s_rows).astype(np.float64)
+    w1n = [to_np(c.w1[e]).astype(np.float64) for e in range(cfg.E)]
+    w3n = [to_np(c.w3[e]).astype(np.float64) for e in range(cfg.E)]
+    w2n = [to_np(c.w2[e]).astype(np.float64) for e in range(cfg.E)]
+    ref_spec, ref_true, ref_dev = O.speculative_execution(
+        sn[toks], p_idx[toks], p_w[toks], t_idx[toks], t_w[toks], np.stack(w1n), np.stack(w3n),
+        np.stack(w2n))
+    assert rel_err_rows(to_np(y_spec)[toks], ref_spec).max() <= VALUE_TOL
+    assert rel_err_rows(to_np(y_true)[toks], ref_true).max() <= VALUE_TOL
+    ys, yt = to_np(y_spec)[toks].astype(np.float64), to_np(y_true)[toks].astype(np.float64)
+    gpu_dev = np.linalg.norm(ys - yt) / np.linalg.norm(yt)
+    assert abs(gpu_dev - ref_dev) <= 0.02 + 0.02 * ref_dev

@@ -574,3 +574,41 @@ def test_inter_never_confident_reduces_to_intra():
     prev = rng.integers(0, P, size=T)
     assert np.array_equal(O.predict_partition_inter(ids, conf, emap, P, K, prev, uni),
                           O.predict_partition(ids, conf, emap, P))
+
+
+def test_speculative_execution_pins():
+    """Identical predicted and true routes give zero deviation; changing one token's one
+    route changes that token's output by exactly the weighted difference of the two
+    experts' outputs (and no other token)."""
+    x, ids, wg, w1, w3, w2, conf, emap = tiny_layer(seed=31, E=8, K=2, S=1)
+    logits = O.gate_logits(x, wg)
+    idx = O.topk_select(logits, 2)
+    w = O.gate_weights(logits, idx)
+    y_spec, y_true, dev = O.speculative_execution(x, idx, w, idx, w, w1, w3, w2, n_shared=1)
+    assert dev == 0.0 and (y_spec == y_true).all()
+    idx2 = idx.copy()
+    old = int(idx2[5, 1])
+    new = (old + 1) % 8 if (old + 1) % 8 != idx2[5, 0] else (old + 2) % 8
+    idx2[5, 1] = new
+    y2, _, dev2 = O.speculative_execution(x, idx2, w, idx, w, w1, w3, w2, n_shared=1)
+    diff = y2 - y_true
+    assert np.abs(np.delete(diff, 5, axis=0)).max() < 1e-12
+    exp = w[5, 1] * (O.swiglu_ffn(x[5:6], w1[new], w3[new], w2[new])[0]
+                     - O.swiglu_ffn(x[5:6], w1[old], w3[old], w2[old])[0])
+    np.testing.assert_allclose(diff[5], exp, rtol=1e-10, atol=1e-12)
+    assert dev2 > 0
+
+
+# ------------------------------------------------- co-clustering (s-EG) ------
+
+
+def test_coclustering_cost_hand():
+    """Two tokens, four experts, two clusters. act: token 0 fires experts 0,1 (3 and 1
+    times), token 1 fires experts 2,3 (2 and 2). Expert map (0,0,1,1) with tokens (0,1):
+    nothing remote, loads 4 and 4 -> cost 0. Tokens (0,0): token 1's 4 activations remote
+    (of 8 = 0.5), loads 8 and 0 -> imbalance (8 - 4)/4 = 1; theta 0.25 -> 0.25 + 0.375."""
+    act = np.array([[3, 1, 0, 0], [0, 0, 2, 2]], float)
+    assert O.coclustering_cost(act, [0, 0, 1, 1], [0, 1], 2, 0.25) == 0.0
+    assert abs(O.coclustering_cost(act, [0, 0, 1, 1], [0, 0], 2, 0.25) - 0.625) < 1e-15
+    # expert map (0,1,0,1): token 0 loses expert 1 (1), token 1 loses expert 2 (2) -> 3/8
+    assert abs(O.coclustering_cost(act, [0, 1, 0, 1], [0, 1], 2, 0.0) - 0.375) < 1e-15
