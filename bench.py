@@ -545,8 +545,8 @@ def run_native(args):
     if os.path.exists(tfile):
         with open(tfile) as f:
             tj = json.load(f)
-        if tj.get("source_hash") == source_hash("ffn.cu") and tj.get("workload") == cfg.name:
-            traffic = tj.get("bytes_per_step")
+        if tj.get("source_hash") == source_hash("ffn.cu"):
+            traffic = tj.get("workloads", {}).get(cfg.name, {}).get("bytes_per_step")
     kernel_name = "expert_ffn (grouped SwiGLU up + down GEMMs)"
     if ffn_flops(cfg) / fbytes >= peak_tf * 1e12 / (hbm * 1e9):
         roofline = {"bound": "tensor", "achieved": round(achieved_tf, 2), "peak": peak_tf,
