@@ -14,7 +14,8 @@
 //           into one of two TMEM accumulators of 256 fp32 columns;
 //   warp 2  allocates and frees the 512 TMEM columns;
 //   warps 4-7 drain an accumulator (tcgen05.ld, one TMEM lane = one row per thread),
-//           apply SwiGLU (up) and store, while the MMAs of the next tile run.
+//           apply SwiGLU (up) and store through a per-warp shared-memory staging tile
+//           (coalesced 128-byte row segments), while the MMAs of the next tile run.
 // In the up GEMM the B stage holds 128 rows of W1 followed by the same 128 rows of
 // W3, so one N = 256 MMA produces the gate and up halves of the tile together.
 // Expert segments are not padded: a tile reaching past its group's last row reads
@@ -34,8 +35,52 @@ constexpr uint32_t kStageA = 128 * 128;  // 128 rows x 128 bytes
 constexpr uint32_t kStageB = 256 * 128;  // 256 rows x 128 bytes
 constexpr int kThreads = 256;
 constexpr int kAccCols = 256;            // fp32 columns per accumulator
-constexpr size_t kSmemBytes =
-    1024 + kStages * (kStageA + kStageB) + 256 + 4 * (kMaxGroups + 1 + 513 + 4);
+constexpr uint32_t kStageOut = 4 * 32 * 128;  // epilogue staging: 4 warps x 32 rows x 128 B
+constexpr size_t kSmemBytes = 1024 + kStages * (kStageA + kStageB) + kStageOut + 256 +
+                              4 * (kMaxGroups + 1 + 513 + 4);
+
+// Epilogue stores. A thread owns one accumulator row, so a direct 16-byte store from a
+// warp touches 32 rows and fills half of each 32-byte sector. Each epilogue warp instead
+// stages its 32 rows x 128 bytes in shared memory (16-byte chunks XOR-swizzled by row,
+// which keeps both the row-wise writes and the column-wise reads free of bank conflicts)
+// and writes them back as 4 rows x 128 contiguous bytes per store instruction.
+template <typename TE>
+struct RowStager {
+  static constexpr int kVec = 16 / (int)sizeof(TE);           // elements per 16 bytes
+  static constexpr int kColsPerFlush = 128 / (int)sizeof(TE);  // columns per staged row
+  uint8_t* buf;    // this warp's 32 x 128 bytes
+  TE* out;         // output matrix, row pitch N elements
+  long long row0;  // output row of the warp's first row
+  int valid;       // leading rows of the 32 that belong to the group
+  int N;
+
+  // 32 values of this lane's row, columns [c, c + 32) (c a multiple of 32)
+  __device__ __forceinline__ void put32(int lane, int c, const float* v) const {
+    const int chunk0 = ((c % kColsPerFlush) * (int)sizeof(TE)) >> 4;
+#pragma unroll
+    for (int j = 0; j < 32 / kVec; ++j) {
+      const int ch = chunk0 + j;
+      *reinterpret_cast<uint4*>(buf + lane * 128 + ((ch ^ (lane & 7)) << 4)) =
+          pack16(v + j * kVec, (const TE*)nullptr);
+    }
+  }
+  // store the staged window, whose first column is col0
+  __device__ __forceinline__ void flush(int lane, int col0) const {
+    __syncwarp();
+    const int ch = lane & 7;
+    const int col = col0 + ch * kVec;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int rr = i * 4 + (lane >> 3);
+      const uint4 v = *reinterpret_cast<const uint4*>(buf + rr * 128 + ((ch ^ (rr & 7)) << 4));
+      if (rr < valid && col + kVec <= N)
+        *reinterpret_cast<uint4*>(out + (size_t)(row0 + rr) * N + col) = v;
+    }
+    __syncwarp();
+  }
+};
+
+__device__ __forceinline__ int clamp_rows(int v) { return v < 0 ? 0 : (v > 32 ? 32 : v); }
 
 // tile_start[g] = first m-tile of group g; tile_start[G] = total m-tiles. expert_off must
 // be non-decreasing from 0 to at most T K; otherwise no tile is scheduled and the status
@@ -149,7 +194,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = base;
   uint8_t* sB = base + kStages * kStageA;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * kStageB);
+  uint8_t* sOut = sB + kStages * kStageB;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + kStageOut);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + 2;
@@ -260,7 +306,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;
-    const int r = q * 32 + lane;  // accumulator row (TMEM lane) of this thread
     uint32_t tcount = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++tcount) {
       Tile tl;
@@ -273,10 +318,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       }
       tc::fence_after_sync();
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + a * kAccCols;
-      const bool row_ok = tl.m0 + r < tl.rows;
-      TE* out = static_cast<TE*>(tl.out_shared ? p.out_sh : p.out);
-      TE* orow = out + (size_t)(tl.out_row + r) * p.N;
-      constexpr int kVec = 16 / (int)sizeof(TE);
+      const RowStager<TE> rs{sOut + q * 4096, static_cast<TE*>(tl.out_shared ? p.out_sh : p.out),
+                             tl.out_row + q * 32, clamp_rows(tl.rows - tl.m0 - q * 32), p.N};
+      constexpr int kWin = RowStager<TE>::kColsPerFlush;
       if (UP) {
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
@@ -284,20 +328,18 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           tc::tmem_ld32(taddr + c, gv);
           tc::tmem_ld32(taddr + 128 + c, uv);
           tc::tmem_ld_wait();
+          if (c == 96) {  // the accumulator is read out: the next tile's MMAs may start
+            tc::fence_before_sync();
+            tc::mbar_arrive(&tempty[a]);
+          }
           float h[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const float gg = __uint_as_float(gv[i]);
             h[i] = gg / (1.0f + __expf(-gg)) * __uint_as_float(uv[i]);
           }
-          if (row_ok) {
-#pragma unroll
-            for (int v = 0; v < 32 / kVec; ++v) {
-              const int n = tl.n0 + c + v * kVec;
-              if (n + kVec <= p.N)
-                *reinterpret_cast<uint4*>(orow + n) = pack16(h + v * kVec, (const TE*)nullptr);
-            }
-          }
+          rs.put32(lane, c, h);
+          if ((c + 32) % kWin == 0) rs.flush(lane, tl.n0 + c + 32 - kWin);
         }
       } else {
 #pragma unroll 1
@@ -305,21 +347,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           uint32_t yv[32];
           tc::tmem_ld32(taddr + c, yv);
           tc::tmem_ld_wait();
+          if (c == 224) {
+            tc::fence_before_sync();
+            tc::mbar_arrive(&tempty[a]);
+          }
           float y[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) y[i] = __uint_as_float(yv[i]);
-          if (row_ok) {
-#pragma unroll
-            for (int v = 0; v < 32 / kVec; ++v) {
-              const int n = tl.n0 + c + v * kVec;
-              if (n + kVec <= p.N)
-                *reinterpret_cast<uint4*>(orow + n) = pack16(y + v * kVec, (const TE*)nullptr);
-            }
-          }
+          rs.put32(lane, c, y);
+          if ((c + 32) % kWin == 0) rs.flush(lane, tl.n0 + c + 32 - kWin);
         }
       }
-      tc::fence_before_sync();
-      tc::mbar_arrive(&tempty[a]);
     }
   }
   tc::fence_before_sync();
@@ -338,8 +376,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 // epilogues drain their own 128 TMEM lanes and arrive on the leader's `tempty`.
 constexpr int kPairStages = 6;
 constexpr uint32_t kPairStage = 128 * 128;  // A half or B half: 128 rows x 128 bytes
-constexpr size_t kPairSmemBytes =
-    1024 + kPairStages * 2 * kPairStage + 256 + 4 * (kMaxGroups + 1 + 513 + 4);
+constexpr size_t kPairSmemBytes = 1024 + kPairStages * 2 * kPairStage + kStageOut + 256 +
+                                  4 * (kMaxGroups + 1 + 513 + 4);
 
 template <bool UP>
 __device__ __forceinline__ void decode_pair_tile(const int32_t* ts, const int32_t* eo,
@@ -391,7 +429,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = base;
   uint8_t* sB = base + kPairStages * kPairStage;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kPairStages * kPairStage);
+  uint8_t* sOut = sB + kPairStages * kPairStage;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + kStageOut);
   uint64_t* empty = full + kPairStages;
   uint64_t* tfull = empty + kPairStages;
   uint64_t* tempty = tfull + 2;
@@ -492,7 +531,6 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- epilogue (both CTAs)
     const int q = warp & 3;
-    const int r = q * 32 + lane;
     uint32_t tcount = 0;
     for (int t = pair; t < total; t += npairs, ++tcount) {
       Tile tl;
@@ -505,9 +543,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
       }
       tc::fence_after_sync();
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + a * kAccCols;
-      const bool row_ok = tl.m0 + r < tl.rows;
-      TE* out = static_cast<TE*>(tl.out_shared ? p.out_sh : p.out);
-      TE* orow = out + (size_t)(tl.out_row + r) * p.N;
+      const RowStager<TE> rs{sOut + q * 4096, static_cast<TE*>(tl.out_shared ? p.out_sh : p.out),
+                             tl.out_row + q * 32, clamp_rows(tl.rows - tl.m0 - q * 32), p.N};
+      constexpr int kWin = RowStager<TE>::kColsPerFlush;
       if (UP) {
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
@@ -515,20 +553,18 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
           tc::tmem_ld32(taddr + c, gv);
           tc::tmem_ld32(taddr + 128 + c, uv);
           tc::tmem_ld_wait();
+          if (c == 96) {  // the accumulator is read out: the next tile's MMAs may start
+            tc::fence_before_sync();
+            tc::mbar_arrive_cluster(tc::cluster_addr(&tempty[a], 0));
+          }
           float h[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const float gg = __uint_as_float(gv[i]);
             h[i] = gg / (1.0f + __expf(-gg)) * __uint_as_float(uv[i]);
           }
-          if (row_ok) {
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const int n = tl.n0 + c + v * 8;
-              if (n + 8 <= p.N)
-                *reinterpret_cast<uint4*>(orow + n) = pack16(h + v * 8, (const TE*)nullptr);
-            }
-          }
+          rs.put32(lane, c, h);
+          if ((c + 32) % kWin == 0) rs.flush(lane, tl.n0 + c + 32 - kWin);
         }
       } else {
 #pragma unroll 1
@@ -536,21 +572,17 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
           uint32_t yv[32];
           tc::tmem_ld32(taddr + c, yv);
           tc::tmem_ld_wait();
+          if (c == 224) {
+            tc::fence_before_sync();
+            tc::mbar_arrive_cluster(tc::cluster_addr(&tempty[a], 0));
+          }
           float y[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) y[i] = __uint_as_float(yv[i]);
-          if (row_ok) {
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const int n = tl.n0 + c + v * 8;
-              if (n + 8 <= p.N)
-                *reinterpret_cast<uint4*>(orow + n) = pack16(y + v * 8, (const TE*)nullptr);
-            }
-          }
+          rs.put32(lane, c, y);
+          if ((c + 32) % kWin == 0) rs.flush(lane, tl.n0 + c + 32 - kWin);
         }
       }
-      tc::fence_before_sync();
-      tc::mbar_arrive_cluster(tc::cluster_addr(&tempty[a], 0));
     }
   }
   tc::fence_before_sync();
