@@ -331,6 +331,21 @@ class Workload:
         rec(6)
 
 
+def plain_topk_hit_rate(wl):
+    """Hit rate of the prefetch predictor when the next router takes a plain top-K over all
+    experts instead of the layer's grouped rule."""
+    import torch
+    s, c, p = wl.smoe, wl.cfg, wl.prefetch
+    desc = s.make_desc(c.T, c.d, c.E, c.K, 1, c.F, c.n_shared, c.P, c.vocab, c.dtype)
+    i32 = dict(dtype=torch.int32, device=wl.dev)
+    pi, ti = torch.empty(c.T, c.K, **i32), torch.empty(c.T, c.K, **i32)
+    hits = torch.zeros(1, dtype=torch.int64, device=wl.dev)
+    s.smoe_prefetch_predict(desc, p["r"], p["d_l"], wl.y, p["gamma"], p["beta"], p["wgn"], pi, ti,
+                            hits, wl.ws)
+    torch.cuda.synchronize()
+    return float(hits.item() / (c.T * c.K))
+
+
 def speculative_execution_report(wl):
     """Run the next layer's stand-in (this layer's experts) on s = LN(r + y) with the
     routes predicted from q and with the true routes; report the hit rate, the relative
@@ -626,8 +641,16 @@ def run_native(args):
             "ms": inter_info["predict_shuffle_inter_ms"]}
     if not args.no_placement:
         result["placement"] = placement_report(wl)
+    if cfg.H > 1:
+        # FoE layout: each token's group copies sit on their groups' partitions
+        lar_f = torch.zeros(4, dtype=torch.int64, device=dev)
+        smoe.smoe_lar(wl.desc, wl.idx, wl.emap_d, lar_f, wl.ws)
+        torch.cuda.synchronize()
+        lf = lar_f.cpu().numpy()
+        result["alpha"]["FoE"] = float(lf[0] / lf[1])
     if wl.prefetch is not None:
         result["prefetch_hit_rate"] = float(wl.prefetch["hits"].item() / (cfg.T * cfg.K))
+        result["prefetch_hit_rate_plain_topk"] = plain_topk_hit_rate(wl)
         result["speculative_execution"] = speculative_execution_report(wl)
     if rank == 0:
         print(json.dumps(result), flush=True)

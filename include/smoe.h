@@ -155,9 +155,9 @@ SMOE_API int smoe_predict_shuffle_inter(const smoe_desc* desc, const int32_t* to
  * whose device memory pool belongs to another framework. The pages have no
  * counterpart; it computes exactly what smoe_predict_shuffle computes, with the same
  * arguments minus the workspace.
- *   - Its histogram scratch is a 256 KB array inside the library that every GPU which
+ *   - Its histogram scratch is a 1 MB array inside the library that every GPU which
  *     loads the library holds until the process exits; T is limited to 1048576 tokens
- *     (1024 tiles of 1024), larger T returns SMOE_ERR_SHAPE.
+ *     (4096 tiles of 256), larger T returns SMOE_ERR_SHAPE.
  *   - It allocates nothing and calls no allocating routine.
  *   - The first call on a device looks up that array's device address (with the
  *     device current); make that first call before any stream capture begins.

@@ -41,20 +41,27 @@ select_kernel(const float* __restrict__ part, int KS, long long split_stride,
     topk_idx = so.idx;
     topk_w = so.w;
   }
+  // split s of every value is loaded before any of split s + 1 is added, so all of a
+  // split's loads (and, unrolled, those of several splits) are in flight together
   float v[kMaxPerLane];
+  const float* prow = part + (size_t)t * E + lane;
+#pragma unroll
+  for (int i = 0; i < kMaxPerLane; ++i) v[i] = lane + 32 * i < E ? prow[32 * i] : -INFINITY;
+#pragma unroll 4
+  for (int s = 1; s < KS; ++s) {
+    const float* ps = prow + (size_t)s * split_stride;
+    float a[kMaxPerLane];
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i) a[i] = lane + 32 * i < E ? ps[32 * i] : 0.0f;
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i) v[i] += a[i];
+  }
   float m = -INFINITY;
 #pragma unroll
   for (int i = 0; i < kMaxPerLane; ++i) {
     const int e = lane + 32 * i;
-    float acc = -INFINITY;
-    if (e < E) {
-      const float* p = part + (size_t)t * E + e;
-      acc = p[0];
-      for (int s = 1; s < KS; ++s) acc += p[(size_t)s * split_stride];
-      if (logits_out) logits_out[(size_t)to * E + e] = acc;
-    }
-    v[i] = acc;
-    m = fmaxf(m, acc);
+    if (e < E && logits_out) logits_out[(size_t)to * E + e] = v[i];
+    m = fmaxf(m, v[i]);
   }
 #pragma unroll
   for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
@@ -104,6 +111,98 @@ select_kernel(const float* __restrict__ part, int KS, long long split_stride,
   if (lane < K) {
     topk_idx[(size_t)to * K + lane] = my_idx;
     topk_w[(size_t)to * K + lane] = my_w;
+  }
+}
+
+// Sub-warp selection: L lanes per token (32 / L tokens per warp), lane j holding experts
+// j, j + L, j + 2L, ... The warp-per-token kernel spends most of its instructions on
+// 5-step butterflies; with L = 8 or 16 lanes a pick takes 3 or 4 steps for 32 / L tokens
+// at once, and the K weights are computed by K lanes together at the end. The picks,
+// their order and the logits are the same as the warp kernel's (the same total order:
+// logit descending, expert index ascending; the same split-order partial sums). Used
+// when K <= L; pick k is held by lane k.
+template <int L, int kPer>
+__global__ void __launch_bounds__(256)
+select_sub_kernel(const float* __restrict__ part, int KS, long long split_stride,
+                  float* __restrict__ logits_out, int T, int E, int K, int H, int renorm,
+                  int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, RouteSplitOut so) {
+  pdl_wait_and_trigger();
+  const int j = threadIdx.x & (L - 1);
+  const int t = (int)((blockIdx.x * blockDim.x + threadIdx.x) / L);
+  const bool valid = t < T;  // every lane stays for the shuffles
+  const bool second = valid && t >= so.split;
+  const int to = second ? t - so.split : t;
+  if (second) {
+    logits_out = so.logits;
+    topk_idx = so.idx;
+    topk_w = so.w;
+  }
+  float v[kPer];
+  const float* prow = part + (size_t)(valid ? t : 0) * E + j;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) v[i] = (valid && j + L * i < E) ? prow[L * i] : -INFINITY;
+#pragma unroll 4
+  for (int s = 1; s < KS; ++s) {
+    const float* ps = prow + (size_t)s * split_stride;
+    float a[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) a[i] = (valid && j + L * i < E) ? ps[L * i] : 0.0f;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) v[i] += a[i];
+  }
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = j + L * i;
+    if (valid && e < E && logits_out) logits_out[(size_t)to * E + e] = v[i];
+    m = fmaxf(m, v[i]);
+  }
+#pragma unroll
+  for (int off = L >> 1; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  float sum = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i)
+    if (j + L * i < E) sum += expf(v[i] - m);
+#pragma unroll
+  for (int off = L >> 1; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+
+  const int per = E / H, kh = K / H;
+  uint32_t taken = 0;
+  float my_v = -INFINITY;
+  int my_i = 0;
+  for (int h = 0; h < H; ++h) {
+    const int lo = h * per, hi = lo + per;
+    for (int q = 0; q < kh; ++q) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int e = j + L * i;
+        if (e >= lo && e < hi && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
+          bv = v[i];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int off = L >> 1; off; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+      }
+      if (bi < E && (bi & (L - 1)) == j) taken |= 1u << (bi / L);
+      if (j == h * kh + q) { my_v = bv; my_i = bi; }
+    }
+  }
+  float w = j < K ? expf(my_v - m) / sum : 0.0f;
+  if (renorm) {
+    float sw = w;
+#pragma unroll
+    for (int off = L >> 1; off; off >>= 1) sw += __shfl_xor_sync(0xffffffffu, sw, off);
+    w = w / sw;
+  }
+  if (valid && j < K) {
+    topk_idx[(size_t)to * K + j] = my_i;
+    topk_w[(size_t)to * K + j] = w;
   }
 }
 
@@ -355,6 +454,24 @@ cudaError_t launch_route(const smoe_desc& d, int rows, const void* x, const void
   }
   float* lo = logits_out == logits_in ? nullptr : logits_out;
   const long long stride = (long long)rows * d.E;
+  if (d.K <= 8 && d.E <= 128) {
+    const int grid = ceil_div(rows * 8, 256);
+    if (d.E <= 32)
+      SMOE_LAUNCH((select_sub_kernel<8, 4>), grid, 256, 0, s, part, KS, stride, lo, rows, d.E,
+                  d.K, d.H, d.renorm, topk_idx, topk_w, so);
+    else if (d.E <= 64)
+      SMOE_LAUNCH((select_sub_kernel<8, 8>), grid, 256, 0, s, part, KS, stride, lo, rows, d.E,
+                  d.K, d.H, d.renorm, topk_idx, topk_w, so);
+    else
+      SMOE_LAUNCH((select_sub_kernel<8, 16>), grid, 256, 0, s, part, KS, stride, lo, rows, d.E,
+                  d.K, d.H, d.renorm, topk_idx, topk_w, so);
+    return cudaGetLastError();
+  }
+  if (d.K <= 16 && d.E <= 256) {
+    SMOE_LAUNCH((select_sub_kernel<16, 16>), ceil_div(rows * 16, 256), 256, 0, s, part, KS,
+                stride, lo, rows, d.E, d.K, d.H, d.renorm, topk_idx, topk_w, so);
+    return cudaGetLastError();
+  }
   const dim3 grid(ceil_div(rows, kSelWarps)), block(kSelWarps * 32);
   if (d.E <= 128)
     SMOE_LAUNCH(select_kernel<4>, grid, block, 0, s, part, KS, stride, lo, rows, d.E, d.K, d.H,

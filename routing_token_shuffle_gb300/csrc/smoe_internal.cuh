@@ -92,7 +92,8 @@ struct WsLayout {
   size_t total;
 };
 
-constexpr int kSortTile = 1024;     // elements per counting-sort tile
+constexpr int kSortTile = 1024;     // pairs per tile of the dispatch counting sort
+constexpr int kShufTile = 256;      // tokens per tile of the shuffle counting sort
 constexpr int kMaxGroups = 520;     // E + n_shared upper bound
 
 bool ws_layout(const smoe_desc& d, WsLayout* out);

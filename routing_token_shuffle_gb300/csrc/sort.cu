@@ -8,7 +8,8 @@
 //
 // A counting sort is three launches with no inter-CTA waiting: per-tile bucket
 // histograms, one CTA scanning the (bucket, tile) table, and a scatter that ranks
-// each tile's elements stably (warp match + per-warp counts in shared memory).
+// each tile's elements stably (warp match + per-warp counts in shared memory). Tiles
+// are 256 tokens for the shuffle and 1024 (token, expert) pairs for the dispatch.
 #include <algorithm>
 #include <mutex>
 
@@ -28,14 +29,15 @@ __device__ __forceinline__ unsigned lanemask_lt() {
 }
 
 // ------------------------------------------------------------------ predict
-// 64 tokens per CTA (a 1024-token sort tile spans 16 CTAs). The CTA stages the 64
-// C_p rows in shared memory in one burst, warp 0 lists each partition's experts in
-// ascending order (warp match), then one warp per token: lane p adds its partition's
-// row entries in that order (one fp32 add each, the oracle's order), and a butterfly
-// argmax with the order (score descending, partition ascending) picks pred[t]. The
-// CTA's partition counts are added to its sort tile's histogram entries (which the
-// launcher zeroes first).
-constexpr int kPredTokens = 64;
+// 32 tokens per CTA (a 256-token shuffle tile spans 8 CTAs). The CTA stages the 32 C_p
+// rows in shared memory with 16-byte loads all in flight at once, warp 0 lists each
+// partition's experts in ascending order (warp match), then each warp scores 32 / P2
+// tokens side by side (P2 = P rounded up to a power of two lanes per token): lane p
+// adds its partition's row entries in that order (one fp32 add each, the oracle's
+// order), and a butterfly argmax over the token's lanes with the order (score
+// descending, partition ascending) picks pred[t]. The CTA's partition counts are added
+// to its tile's histogram entries (which the launcher zeroes first).
+constexpr int kPredTokens = 32;
 
 // INTER: the inter-layer source of "Speculative MoE" §4.1 also votes. prev[t] is the
 // token's cluster at the previous layer and table_a [P, P] the 2-gram table A; A's row
@@ -73,10 +75,24 @@ predict_hist_kernel(const int32_t* __restrict__ ids, const float* __restrict__ c
     s_id[tid] = ok ? id : -1;
   }
   __syncthreads();
-  for (int k = tid; k < n * E; k += kThreads) {
-    const int i = k / E, e = k - i * E;
-    const int id = s_id[i];
-    s_rows[k] = id >= 0 ? __ldg(conf + (size_t)id * E + e) : 0.0f;
+  if ((E & 3) == 0) {
+    const int q = E >> 2;  // 16-byte vectors per row
+    const int nv = n * q;
+    float4* dst = reinterpret_cast<float4*>(s_rows);
+#pragma unroll 4
+    for (int k = tid; k < nv; k += kThreads) {
+      const int i = k / q, c = k - i * q;
+      const int id = s_id[i];
+      dst[k] = id >= 0 ? __ldg(reinterpret_cast<const float4*>(conf + (size_t)id * E) + c)
+                       : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+  } else {
+#pragma unroll 4
+    for (int k = tid; k < n * E; k += kThreads) {
+      const int i = k / E, e = k - i * E;
+      const int id = s_id[i];
+      s_rows[k] = id >= 0 ? __ldg(conf + (size_t)id * E + e) : 0.0f;
+    }
   }
   if (warp == 0) {
     // partition p's experts in ascending order: s_list[s_start[p] .. s_start[p+1])
@@ -110,47 +126,57 @@ predict_hist_kernel(const int32_t* __restrict__ ids, const float* __restrict__ c
     }
   }
   __syncthreads();
-  for (int i = warp; i < n; i += kWarps) {
-    const float* row = s_rows + (size_t)i * E;
+  int P2 = 1;
+  while (P2 < P) P2 <<= 1;
+  const int G = 32 / P2;                       // tokens per warp pass
+  const int sub = lane / P2, pl = lane - sub * P2;
+  for (int i0 = warp * G; i0 < n; i0 += kWarps * G) {
+    const int i = i0 + sub;
+    const bool tok = i < n;
     float sc = -INFINITY;
-    if (lane < P) {
+    if (tok && pl < P) {
+      const float* row = s_rows + (size_t)i * E;
+      const int j1 = s_start[pl + 1];
       float acc = 0.0f;
-      for (int j = s_start[lane]; j < s_start[lane + 1]; ++j) acc = acc + row[s_list[j]];
+#pragma unroll 4
+      for (int j = s_start[pl]; j < j1; ++j) acc = acc + row[s_list[j]];
       sc = acc;
     }
-    int bi = lane;
-#pragma unroll
-    for (int off = 16; off; off >>= 1) {
+    int bi = pl;
+    for (int off = P2 >> 1; off; off >>= 1) {
       const float os = __shfl_xor_sync(0xffffffffu, sc, off);
       const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
       if (os > sc || (os == sc && oi < bi)) { sc = os; bi = oi; }
     }
     // an invalid id, or a NaN/inf row (outside the contract), gives partition 0
-    int best = (s_id[i] >= 0 && (unsigned)bi < (unsigned)P) ? bi : 0;
-    if (INTER && s_id[i] >= 0) {
-      int c = prev[t0 + i];
-      if ((unsigned)c >= (unsigned)P) {
-        if (lane == 0) record_error(st, kStatusData, kBadSrcPart, t0 + i);
-        c = 0;
+    const bool id_ok = tok && s_id[i] >= 0;
+    int best = (id_ok && (unsigned)bi < (unsigned)P) ? bi : 0;
+    if (INTER) {
+      int c = 0;
+      if (id_ok) {
+        c = prev[t0 + i];
+        if ((unsigned)c >= (unsigned)P) {
+          if (pl == 0) record_error(st, kStatusData, kBadSrcPart, t0 + i);
+          c = 0;
+        }
       }
-      float av = lane < P ? table_a[c * P + lane] : -INFINITY;
-      int ai = lane;
-#pragma unroll
-      for (int off = 16; off; off >>= 1) {
+      float av = (id_ok && pl < P) ? table_a[c * P + pl] : -INFINITY;
+      int ai = pl;
+      for (int off = P2 >> 1; off; off >>= 1) {
         const float ov = __shfl_xor_sync(0xffffffffu, av, off);
         const int oi = __shfl_xor_sync(0xffffffffu, ai, off);
         if (ov > av || (ov == av && oi < ai)) { av = ov; ai = oi; }
       }
       const float conf_intra = sc / (float)K;
-      if (av > conf_intra && (unsigned)ai < (unsigned)P) best = ai;
+      if (id_ok && av > conf_intra && (unsigned)ai < (unsigned)P) best = ai;
     }
-    if (lane == 0) {
+    if (tok && pl == 0) {
       pred[t0 + i] = best;
       atomicAdd(&s_cnt[best], 1);
     }
   }
   __syncthreads();
-  if (tid < P && s_cnt[tid] > 0) atomicAdd(&hist[tid * ntiles + t0 / kSortTile], s_cnt[tid]);
+  if (tid < P && s_cnt[tid] > 0) atomicAdd(&hist[tid * ntiles + t0 / kShufTile], s_cnt[tid]);
 }
 
 size_t predict_smem(int E) { return sizeof(float) * kPredTokens * E; }
@@ -169,6 +195,7 @@ dispatch_hist_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict_
   const long long n = (long long)T * K;
   const long long q0 = (long long)blockIdx.x * kSortTile;
   const long long q1 = min(q0 + kSortTile, n);
+#pragma unroll 4
   for (long long q = q0 + tid; q < q1; q += kThreads) {
     const int s = (int)(q / K), k = (int)(q - (long long)s * K);
     const int t = perm ? perm[s] : s;
@@ -196,37 +223,50 @@ __global__ void __launch_bounds__(1024)
 scan_kernel(const int32_t* __restrict__ hist, int32_t* __restrict__ offs, int L, int B,
             int ntiles, int n, int32_t* __restrict__ bucket_off) {
   pdl_wait_and_trigger();
+  // rounds of 4096 entries: each thread loads 4 consecutive counts with one 16-byte
+  // load, the block scans the per-thread sums, a running carry links the rounds
   __shared__ int s_warp[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int per = (L + blockDim.x - 1) / blockDim.x;
-  const int lo = min(tid * per, L), hi = min(lo + per, L);
-  int sum = 0;
-  for (int i = lo; i < hi; ++i) sum += hist[i];
-  int x = sum;
+  int carry = 0;
+  for (int base = 0; base < L; base += 4096) {
+    const int i = base + tid * 4;
+    int v[4] = {0, 0, 0, 0};
+    if (i + 3 < L) {
+      const int4 q = *reinterpret_cast<const int4*>(hist + i);
+      v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+    } else {
 #pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, x, off);
-    if (lane >= off) x += y;
-  }
-  if (lane == 31) s_warp[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int v = lane < (int)(blockDim.x >> 5) ? s_warp[lane] : 0;
+      for (int j = 0; j < 4; ++j)
+        if (i + j < L) v[j] = hist[i + j];
+    }
+    const int sum = v[0] + v[1] + v[2] + v[3];
+    int x = sum;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, v, off);
-      if (lane >= off) v += y;
+      const int y = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += y;
     }
-    s_warp[lane] = v;
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int w = lane < (int)(blockDim.x >> 5) ? s_warp[lane] : 0;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, off);
+        if (lane >= off) w += y;
+      }
+      s_warp[lane] = w;
+    }
+    __syncthreads();
+    int run = carry + x - sum + (warp > 0 ? s_warp[warp - 1] : 0);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (i + j < L) offs[i + j] = run;
+      run += v[j];
+    }
+    carry += s_warp[31];
+    __syncthreads();
   }
-  __syncthreads();
-  int run = x - sum + (warp > 0 ? s_warp[warp - 1] : 0);
-  for (int i = lo; i < hi; ++i) {
-    const int v = hist[i];
-    offs[i] = run;
-    run += v;
-  }
-  __syncthreads();
   for (int b = tid; b < B; b += blockDim.x) bucket_off[b] = offs[b * ntiles];
   if (tid == 0) bucket_off[B] = n;
 }
@@ -239,7 +279,7 @@ enum ScatterMode { kShuffle = 0, kDispatch = 1 };
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads)
-scatter_kernel(const int32_t* __restrict__ bucket, int n, int B, int ntiles,
+scatter_kernel(const int32_t* __restrict__ bucket, int n, int B, int ntiles, int tile,
                const int32_t* __restrict__ offs,
                // kShuffle: perm_out[pos] = i
                int32_t* __restrict__ perm_out,
@@ -256,8 +296,8 @@ scatter_kernel(const int32_t* __restrict__ bucket, int n, int B, int ntiles,
     for (int w = 0; w < kWarps; ++w) s_wc[w][b] = 0;
   }
   __syncthreads();
-  const int base = blockIdx.x * kSortTile;
-  for (int c = 0; c < kSortTile && base + c < n; c += kThreads) {
+  const int base = blockIdx.x * tile;
+  for (int c = 0; c < tile && base + c < n; c += kThreads) {
     const int i = base + c + tid;
     const bool valid = i < n;
     const int b = valid ? bucket[i] : -1;
@@ -455,7 +495,7 @@ cudaError_t launch_predict_shuffle(const smoe_desc& d, const int32_t* ids, const
   DeviceStatus* st = ws_ptr<DeviceStatus>(ws, L.status);
   int32_t* hist = ws_ptr<int32_t>(ws, L.sort_hist);
   int32_t* offs = ws_ptr<int32_t>(ws, L.sort_off);
-  const int ntiles = ceil_div(d.T, kSortTile);
+  const int ntiles = ceil_div(d.T, kShufTile);
   cudaError_t e = cudaMemsetAsync(hist, 0, sizeof(int32_t) * d.P * ntiles, s);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(predict_hist_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -473,8 +513,8 @@ cudaError_t launch_predict_shuffle(const smoe_desc& d, const int32_t* ids, const
         predict_smem(d.E), s, ids, conf, emap, d.T, d.E, d.P, d.vocab, pred, hist, ntiles, st,
         nullptr, nullptr, d.K);
   SMOE_LAUNCH(scan_kernel, 1, 1024, 0, s, hist, offs, d.P * ntiles, d.P, ntiles, d.T, part_off);
-  SMOE_LAUNCH(scatter_kernel<kShuffle>, ntiles, kThreads, 0, s, pred, d.T, d.P, ntiles, offs, perm,
-      nullptr, 0, 0, nullptr, nullptr, nullptr);
+  SMOE_LAUNCH(scatter_kernel<kShuffle>, ntiles, kThreads, 0, s, pred, d.T, d.P, ntiles, kShufTile,
+      offs, perm, nullptr, 0, 0, nullptr, nullptr, nullptr);
   if (x_shuf) {
     const int vec = (int)(d.d * elem_size(d) / 16);
     SMOE_LAUNCH(gather_rows_kernel, grid_for_rows(d.T), kThreads, 0, s,
@@ -501,8 +541,8 @@ cudaError_t launch_dispatch(const smoe_desc& d, const int32_t* idx, const int32_
   SMOE_LAUNCH(dispatch_hist_kernel, ntiles, kThreads, 0, s, idx, perm, d.T, d.K, d.E, bucket, hist,
       ntiles, st);
   SMOE_LAUNCH(scan_kernel, 1, 1024, 0, s, hist, offs, d.E * ntiles, d.E, ntiles, n, expert_off);
-  SMOE_LAUNCH(scatter_kernel<kDispatch>, ntiles, kThreads, 0, s, bucket, n, d.E, ntiles, offs,
-      nullptr, perm, d.T, d.K, pair_row, row_token, row_src);
+  SMOE_LAUNCH(scatter_kernel<kDispatch>, ntiles, kThreads, 0, s, bucket, n, d.E, ntiles,
+      kSortTile, offs, nullptr, perm, d.T, d.K, pair_row, row_token, row_src);
   if (x_disp) {
     const int vec = (int)(d.d * elem_size(d) / 16);
     SMOE_LAUNCH(gather_rows_kernel, grid_for_rows(n), kThreads, 0, s,
@@ -546,7 +586,7 @@ cudaError_t launch_lar(const smoe_desc& d, const int32_t* idx, const int32_t* sr
 namespace smoe {
 namespace {
 
-constexpr int kNoAllocMaxTiles = 1024;                        // T <= 1024 * kSortTile
+constexpr int kNoAllocMaxTiles = 4096;                        // T <= 4096 * kShufTile
 constexpr int kNoAllocScratchInts = 2 * 32 * kNoAllocMaxTiles;  // hist + offs for P <= 32
 static __device__ __align__(256) int32_t g_shuffle_scratch[kNoAllocScratchInts];
 
@@ -595,7 +635,7 @@ extern "C" SMOE_API int smoe_predict_shuffle_noalloc(const smoe_desc* desc,
   }
   if (x_shuf != nullptr && (x == nullptr || !aligned16_ptr(x) || !aligned16_ptr(x_shuf)))
     return set_last_error(SMOE_ERR_ARG, "x_shuf needs a 16-byte aligned x");
-  const int ntiles = ceil_div(desc->T, kSortTile);
+  const int ntiles = ceil_div(desc->T, kShufTile);
   if (ntiles > kNoAllocMaxTiles)
     return set_last_error(SMOE_ERR_SHAPE,
                           "smoe_predict_shuffle_noalloc supports at most 1048576 tokens");
@@ -625,7 +665,7 @@ extern "C" SMOE_API int smoe_predict_shuffle_noalloc(const smoe_desc* desc,
   SMOE_LAUNCH_STATUS(scan_kernel, 1, 1024, 0, s, hist, offs, d.P * ntiles, d.P, ntiles, d.T,
       part_off);
   SMOE_LAUNCH_STATUS(scatter_kernel<kShuffle>, ntiles, kThreads, 0, s, pred_part, d.T, d.P, ntiles,
-      offs, shuf_perm, nullptr, 0, 0, nullptr, nullptr, nullptr);
+      kShufTile, offs, shuf_perm, nullptr, 0, 0, nullptr, nullptr, nullptr);
   if (x_shuf) {
     const int vec = (int)(d.d * elem_size(d) / 16);
     SMOE_LAUNCH_STATUS(gather_rows_kernel, grid_for_rows(d.T), kThreads, 0, s,
