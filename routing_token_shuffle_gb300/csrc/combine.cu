@@ -1,15 +1,16 @@
 // Weighted combine back into original token order ("Speculative MoE" §1: expert
 // results return to the token's source; FoE: per-group results are summed).
 //
-// One CTA per token row, threads striding over 16-byte vectors; every element is
-// accumulated in fp32 in the fixed order k = 0..K-1 then shared experts j = 0..S-1
-// and written once: deterministic, no atomics.
+// One CTA per token row, threads striding over 16-byte vectors, up to 8 rows' loads in
+// flight per thread; every element is accumulated in fp32 in the fixed order
+// k = 0..K-1 then shared experts j = 0..S-1 and written once: deterministic, no atomics.
 #include "smoe_internal.cuh"
 
 namespace smoe {
 namespace {
 
 constexpr int kThreads = 128;
+constexpr int kBatch = 8;  // row loads in flight per thread
 
 template <typename TE>
 __global__ void __launch_bounds__(kThreads)
@@ -34,22 +35,39 @@ combine_kernel(const uint4* __restrict__ y_disp, const int32_t* __restrict__ pai
     float acc[V];
 #pragma unroll
     for (int i = 0; i < V; ++i) acc[i] = 0.0f;
-    for (int k = 0; k < K; ++k) {
-      const int r = s_row[k];
-      if (r < 0) continue;
-      const uint4 u = __ldg(y_disp + (size_t)r * nvec + v);
-      float f[V];
-      unpack16(u, f, tag);
-      const float wk = s_w[k];
+    // batches of kBatch rows: all of a batch's loads are issued before the first
+    // accumulation, which still runs in the order k = 0, 1, ...
+    for (int k0 = 0; k0 < K; k0 += kBatch) {
+      uint4 u[kBatch];
 #pragma unroll
-      for (int i = 0; i < V; ++i) acc[i] = fmaf(wk, f[i], acc[i]);
+      for (int b = 0; b < kBatch; ++b) {
+        const int r = k0 + b < K ? s_row[k0 + b] : -1;
+        u[b] = r >= 0 ? __ldg(y_disp + (size_t)r * nvec + v) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        if (k0 + b >= K || s_row[k0 + b] < 0) continue;
+        float f[V];
+        unpack16(u[b], f, tag);
+        const float wk = s_w[k0 + b];
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[i] = fmaf(wk, f[i], acc[i]);
+      }
     }
-    for (int j = 0; j < S; ++j) {
-      const uint4 u = __ldg(y_sh + ((size_t)j * T + t) * nvec + v);
-      float f[V];
-      unpack16(u, f, tag);
+    for (int j0 = 0; j0 < S; j0 += kBatch) {
+      uint4 u[kBatch];
 #pragma unroll
-      for (int i = 0; i < V; ++i) acc[i] += f[i];
+      for (int b = 0; b < kBatch; ++b)
+        u[b] = j0 + b < S ? __ldg(y_sh + ((size_t)(j0 + b) * T + t) * nvec + v)
+                          : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        if (j0 + b >= S) continue;
+        float f[V];
+        unpack16(u[b], f, tag);
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[i] += f[i];
+      }
     }
     y[(size_t)t * nvec + v] = pack16(acc, tag);
   }
