@@ -376,7 +376,6 @@ static int layer_forward_impl(const smoe_desc* d, const smoe_layer_weights* W,
                               const smoe_layer_io* io, void* ws, cudaStream_t s) {
   WsLayout L;
   ws_layout(*d, &L);
-  const size_t TK = (size_t)d->T * d->K;
   float* logits = io->logits ? io->logits : ws_ptr<float>(ws, L.logits);
   int32_t* idx = io->topk_idx ? io->topk_idx : ws_ptr<int32_t>(ws, L.idx);
   float* w = io->topk_w ? io->topk_w : ws_ptr<float>(ws, L.w);
