@@ -11,9 +11,10 @@
 // fp32 layers keep an exact fp32-FMA gate GEMM: the tensor cores would round the
 // operands to tf32 and move logits by ~1e-3, enough to flip routing decisions.
 //
-// Selection: one warp per token, the token's fp32 logits spread over the lanes;
-// each pick is a butterfly argmax under the total order (logit descending, expert
-// index ascending), so equal logits (including +0 / -0) go to the lower index.
+// Selection: 8 or 16 lanes per token (one warp per token when E > 256 or K > 16), the
+// token's fp32 logits spread over those lanes; each pick is a butterfly argmax under the
+// total order (logit descending, expert index ascending), so equal logits (including
+// +0 / -0) go to the lower index.
 #include <algorithm>
 
 #include "tc_common.cuh"
