@@ -1,5 +1,6 @@
 // C entry points: host-side validation, workspace layout and launch sequencing.
 #include <algorithm>
+#include <atomic>
 #include <climits>
 #include <cstdarg>
 #include <cstdio>
@@ -35,20 +36,19 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // The library carries sm_103a code only.
 int check_device() {
-  static int cached[64] = {0};  // 0 unknown, 1 ok, -1 unsupported
+  static std::atomic<int> cached[64];  // 0 unknown, 1 ok (zero-initialised: static storage)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (dev >= 0 && dev < 64 && cached[dev] == 1) return SMOE_OK;
+  const bool slot = dev >= 0 && dev < 64;
+  if (slot && cached[dev].load(std::memory_order_relaxed) == 1) return SMOE_OK;
   int major = 0, minor = 0;
   cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
   cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-  if (major != 10 || minor != 3) {
-    if (dev >= 0 && dev < 64) cached[dev] = -1;
+  if (major != 10 || minor != 3)
     return fail(SMOE_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a",
                 dev, major, minor);
-  }
-  if (dev >= 0 && dev < 64) cached[dev] = 1;
+  if (slot) cached[dev].store(1, std::memory_order_relaxed);
   return SMOE_OK;
 }
 
