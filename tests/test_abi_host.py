@@ -103,3 +103,30 @@ def test_grouped_source_rule_needs_divisibility(lib):
     d = base_desc(E=12, K=3, H=3, P=4)
     n = B.workspace_size(d)
     assert lib.smoe_lar(ctypes.byref(d), 16, None, 16, 16, 256, n, None) == -2
+
+
+def test_newer_entry_points_validate_on_the_host(lib):
+    """Missing or misaligned required pointers are rejected before any CUDA call by the
+    inter-layer, routed-forward, prefetch and combine entry points."""
+    d = base_desc()
+    n = B.workspace_size(d)
+    D = ctypes.byref(d)
+    # smoe_token_cluster(desc, topk_idx, expert_part, cluster, ws, ws_bytes, stream)
+    assert lib.smoe_token_cluster(D, None, 16, 16, 256, n, None) == -1
+    assert lib.smoe_token_cluster(D, 16 + 8, 16, 16, 256, n, None) == -3
+    # smoe_predict_shuffle_inter(desc, ids, conf, map, prev, table_a, x, pred, perm, off,
+    #                            x_shuf, ws, ws_bytes, stream)
+    assert lib.smoe_predict_shuffle_inter(D, 16, 16, 16, None, 16, None, 16, 16, 16, None, 256,
+                                          n, None) == -1
+    assert lib.smoe_predict_shuffle_inter(D, 16, 16, 16, 16, 16 + 4, None, 16, 16, 16, None, 256,
+                                          n, None) == -3
+    # smoe_moe_forward_routed(desc, x, idx, w, w1, w3, w2, y, ws, ws_bytes, stream)
+    assert lib.smoe_moe_forward_routed(D, 16, 16, 16, 16, 16, None, 16, 256, n, None) == -1
+    assert lib.smoe_moe_forward_routed(D, 16, 16, 16, 16, 16, 16, 16, None, n, None) == -4
+    # smoe_prefetch_predict(desc, r, d_l, y, gamma, beta, w_gate_next, logits_q, logits_s,
+    #                       pred_idx, true_idx, hits, qs_out, ws, ws_bytes, stream)
+    assert lib.smoe_prefetch_predict(D, None, 16, 16, 16, 16, 16, None, None, 16, 16, 16, None,
+                                     256, n, None) == -1
+    # smoe_combine(desc, y_disp, pair_row, topk_w, y_shared, y_out, ws, ws_bytes, stream)
+    assert lib.smoe_combine(D, 16, 16 + 4, 16, None, 16, 256, n, None) == -3
+    assert lib.smoe_combine(D, 16, 16, 16, None, None, 256, n, None) == -1
