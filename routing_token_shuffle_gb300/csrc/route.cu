@@ -258,7 +258,7 @@ gate_gemm_f32_kernel(const float* __restrict__ x, const float* __restrict__ wg,
 // A 128 x 64 and B E_pad x 64 bf16 tiles, 128-byte swizzle); warp 1: tcgen05.mma
 // issuer (one N = E_pad MMA per 16-wide K step, two when E_pad > 256); warp 2: TMEM
 // allocation; warps 4-7: write the split's fp32 partial logits, one row per thread.
-constexpr int kGateStages = 3;
+constexpr int kGateMaxStages = 3;  // 2 when E > 256 (a 64 KB B stage)
 constexpr uint32_t kGateA = 128 * 128;
 
 struct GateArgs {
@@ -269,6 +269,7 @@ struct GateArgs {
   uint32_t box_rows;        // B box rows (E_pad, or 256 when E_pad > 256)
   uint32_t b_stage;         // bytes of one B stage
   uint32_t tmem_cols;
+  uint32_t stages;          // ring depth: 3, or 2 when a B stage is 64 KB
 };
 
 __global__ void __launch_bounds__(256, 1)
@@ -279,10 +280,11 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = base;
-  uint8_t* sB = base + kGateStages * kGateA;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kGateStages * p.b_stage);
-  uint64_t* empty = full + kGateStages;
-  uint64_t* tfull = empty + kGateStages;
+  const uint32_t nst = p.stages;
+  uint8_t* sB = base + nst * kGateA;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + nst * p.b_stage);
+  uint64_t* empty = full + kGateMaxStages;
+  uint64_t* tfull = empty + kGateMaxStages;
   uint64_t* drain = tfull + 1;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 1);
   int* s_abort = reinterpret_cast<int*>(s_tmem + 1);
@@ -293,7 +295,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
   const int kb1 = (int)((long long)(ks + 1) * p.nkb / p.KS);
   const bool two = p.E_pad > 256;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kGateStages; ++s) {
+    for (uint32_t s = 0; s < nst; ++s) {
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
@@ -319,7 +321,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     bool ok = true;
     const uint32_t tx = kGateA + (two ? 2u : 1u) * p.box_rows * 128u;
     for (int kb = kb0; kb < kb1; ++kb, ++it) {
-      const uint32_t s = it % kGateStages, ph = (it / kGateStages) & 1u;
+      const uint32_t s = it % nst, ph = (it / nst) & 1u;
       if (!tc::mbar_wait(&empty[s], ph ^ 1u, abort)) { ok = false; break; }
       tc::mbar_expect_tx(&full[s], tx);
       tc::tma_load_2d(sA + s * kGateA, &tmX, &full[s], kb * 64, m0);
@@ -330,15 +332,15 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
       *abort = 1;
       record_error(p.st, kStatusTimeout, kTimeoutGemm, blockIdx.x);
       volatile int never = 0;
-      const uint32_t first = it > (uint32_t)kGateStages ? it - kGateStages : 0;
+      const uint32_t first = it > nst ? it - nst : 0;
       for (uint32_t j = first; j < it; ++j)
-        tc::mbar_wait(&full[j % kGateStages], (j / kGateStages) & 1u, &never);
+        tc::mbar_wait(&full[j % nst], (j / nst) & 1u, &never);
     }
   } else if (warp == 1 && lane == 0) {
     uint32_t it = 0;
     bool ok = true;
     for (int kb = kb0; kb < kb1; ++kb, ++it) {
-      const uint32_t s = it % kGateStages, ph = (it / kGateStages) & 1u;
+      const uint32_t s = it % nst, ph = (it / nst) & 1u;
       if (!tc::mbar_wait(&full[s], ph, abort)) { ok = false; break; }
       tc::fence_after_sync();
       const uint64_t adesc = tc::sw128_kmajor_desc(tc::smem_u32(sA + s * kGateA));
@@ -445,7 +447,8 @@ cudaError_t launch_route(const smoe_desc& d, int rows, const void* x, const void
       if (!encode_tmap_2d(&tX, x, false, rows, d.d, 128, 64)) return cudaErrorInvalidValue;
       if (!encode_tmap_2d(&tW, w_gate, false, d.E, d.d, a.box_rows, 64))
         return cudaErrorInvalidValue;
-      const size_t smem = 1024 + kGateStages * (kGateA + a.b_stage) + 128;
+      a.stages = E_pad > 256 ? 2u : 3u;
+      const size_t smem = 1024 + a.stages * (kGateA + a.b_stage) + 128;
       cudaError_t e = cudaFuncSetAttribute(gate_tc_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;

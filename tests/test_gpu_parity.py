@@ -551,3 +551,63 @@ def test_speculative_execution_qwen3():
     ys, yt = to_np(y_spec)[toks].astype(np.float64), to_np(y_true)[toks].astype(np.float64)
     gpu_dev = np.linalg.norm(ys - yt) / np.linalg.norm(yt)
     assert abs(gpu_dev - ref_dev) <= 0.02 + 0.02 * ref_dev
+
+
+LIMIT_SHAPES = [
+    # T, d, E, K, H, F, S, P, vocab, dtype
+    (300, 64, 512, 32, 1, 64, 8, 32, 1000, "bf16"),   # every size limit at once
+    (129, 8, 16, 16, 16, 8, 1, 3, 50, "f32"),         # d = F = 8: one partial k-block
+    (1, 128, 8, 2, 1, 256, 0, 2, 10, "bf16"),          # a single token
+    (2048, 256, 64, 8, 8, 128, 2, 8, 700, "bf16"),     # grouped routing with shared experts
+    (4096, 128, 8, 2, 2, 384, 1, 4, 300, "bf16"),      # two-SM tiles with a shared expert
+]
+
+
+@pytest.mark.parametrize("T,d,E,K,H,F,S,P,V,dt", LIMIT_SHAPES,
+                         ids=[f"T{s[0]}-d{s[1]}-E{s[2]}-K{s[3]}-H{s[4]}-S{s[6]}-P{s[7]}-{s[9]}"
+                              for s in LIMIT_SHAPES])
+def test_layer_forward_at_limits(T, d, E, K, H, F, S, P, V, dt):
+    """The whole layer at the ABI's limits (E = 512, K = 32, P = 32, 8 shared experts),
+    at the smallest d and F, at T = 1 and with grouped routing: indices bit-exact given the
+    GPU's logits, values against the oracle's own routing."""
+    rng = np.random.default_rng(T + E + K)
+    tdt = torch.float32 if dt == "f32" else torch.bfloat16
+    def t(a):
+        return torch.as_tensor(np.asarray(a, np.float32)).to(tdt).cuda().contiguous()
+    x = t(rng.standard_normal((T, d)))
+    wg = t(rng.standard_normal((E, d)) / np.sqrt(d))
+    w1 = t(rng.standard_normal((E + S, F, d)) / np.sqrt(d))
+    w3 = t(rng.standard_normal((E + S, F, d)) / np.sqrt(d))
+    w2 = t(rng.standard_normal((E + S, d, F)) / np.sqrt(F))
+    conf = rng.random((V, E)).astype(np.float32)
+    conf = (conf / conf.sum(1, keepdims=True) * K).astype(np.float32)
+    emap = rng.integers(0, P, size=E).astype(np.int32)
+    ids = rng.integers(0, V, size=T).astype(np.int32)
+    desc = smoe.make_desc(T, d, E, K, H, F, S, P, V, dt)
+    ws = smoe.workspace(desc)
+    outs = dict(logits=f32(T, E), topk_idx=i32(T, K), topk_w=f32(T, K), pred_part=i32(T),
+                shuf_perm=i32(T), part_off=i32(P + 1), expert_off=i32(E + 1),
+                pair_row=i32(T, K), row_token=i32(T * K),
+                lar=torch.empty(4, dtype=torch.int64, device="cuda"))
+    y = torch.empty_like(x)
+    conf_d = torch.as_tensor(conf, device="cuda")
+    emap_d = torch.as_tensor(emap, device="cuda")
+    ids_d = torch.as_tensor(ids, device="cuda")
+    W = smoe.layer_weights(wg, w1, w3, w2, conf_d, emap_d)
+    smoe.smoe_layer_forward(desc, W, smoe.layer_io(x, ids_d, y, **outs), ws)
+    smoe.smoe_get_status(ws)
+    torch.cuda.synchronize()
+    xn, wgn = to_np(x).astype(np.float64), to_np(wg).astype(np.float64)
+    w1n, w3n, w2n = (to_np(m).astype(np.float64) for m in (w1, w3, w2))
+    ref = O.layer_forward(xn, ids, wgn, w1n, w3n, w2n, conf, emap, K=K, H=H, P=P, n_shared=S,
+                          logits=to_np(outs["logits"]))
+    for k, name in (("topk_idx", "idx"), ("pred_part", "pred"), ("shuf_perm", "shuf_perm"),
+                    ("part_off", "part_off"), ("expert_off", "expert_off"),
+                    ("pair_row", "pair_row"), ("row_token", "row_token")):
+        assert np.array_equal(to_np(outs[k]), ref[name]), k
+    assert np.array_equal(to_np(outs["lar"]).astype(np.uint64), ref["lar"])
+    own = O.layer_forward(xn, ids, wgn, w1n, w3n, w2n, conf, emap, K=K, H=H, P=P, n_shared=S)
+    keep = O.selection_margin(own["logits"], K, H) >= MARGIN
+    assert keep.mean() > 0.5
+    err = rel_err_rows(to_np(y)[keep], own["y"][keep])
+    assert err.max() <= VALUE_TOL, err.max()
