@@ -611,3 +611,42 @@ def test_layer_forward_at_limits(T, d, E, K, H, F, S, P, V, dt):
     assert keep.mean() > 0.5
     err = rel_err_rows(to_np(y)[keep], own["y"][keep])
     assert err.max() <= VALUE_TOL, err.max()
+
+
+@pytest.mark.parametrize("T,E,K,S,d,F,skew", [(3000, 8, 2, 0, 200, 328, True),
+                                               (2600, 8, 2, 1, 200, 328, False),
+                                               (700, 16, 4, 2, 136, 72, True)])
+def test_expert_ffn_skewed_and_odd_sizes(T, E, K, S, d, F, skew):
+    """Expert FFN + combine with d and F not multiples of 64 (partial k-blocks and a
+    partial last n-tile, two-SM and single-SM tiles) and with every token routed to the
+    same K experts (the other experts get no rows)."""
+    g = torch.Generator(device="cuda").manual_seed(T + d)
+    x = torch.randn(T, d, generator=g, device="cuda").to(torch.bfloat16)
+    w1 = (torch.randn(E + S, F, d, generator=g, device="cuda") / d ** 0.5).to(torch.bfloat16)
+    w3 = (torch.randn(E + S, F, d, generator=g, device="cuda") / d ** 0.5).to(torch.bfloat16)
+    w2 = (torch.randn(E + S, d, F, generator=g, device="cuda") / F ** 0.5).to(torch.bfloat16)
+    logits = torch.randn(T, E, generator=g, device="cuda")
+    if skew:
+        logits[:, :K] += 100.0        # experts 0..K-1 win for every token
+    desc = smoe.make_desc(T, d, E, K, 1, F, S, 2, 100, "bf16")
+    ws = smoe.workspace(desc)
+    idx, w = i32(T, K), f32(T, K)
+    smoe.smoe_route(desc, None, None, idx, w, logits_in=logits, ws=ws)
+    eo, pr, rt = i32(E + 1), i32(T, K), i32(T * K)
+    xd = torch.empty(T * K, d, dtype=torch.bfloat16, device="cuda")
+    smoe.smoe_dispatch(desc, idx, eo, pr, rt, ws, x_src=x, x_disp=xd)
+    yd = torch.empty_like(xd)
+    ysh = torch.empty(S, T, d, dtype=torch.bfloat16, device="cuda") if S else None
+    smoe.smoe_expert_ffn(desc, xd, eo, w1, w3, w2, yd, ws, x=x, y_shared=ysh)
+    y = torch.empty_like(x)
+    smoe.smoe_combine(desc, yd, pr, w, y, ws, y_shared=ysh)
+    smoe.smoe_get_status(ws)
+    torch.cuda.synchronize()
+    if skew:
+        assert (np.diff(to_np(eo))[K:] == 0).all()
+    xn = to_np(x).astype(np.float64)
+    W = [tuple(to_np(m[e]).astype(np.float64) for m in (w1, w3, w2)) for e in range(E + S)]
+    ref = O.moe_output(xn, to_np(idx), to_np(w).astype(np.float64),
+                       np.stack([a for a, _, _ in W]), np.stack([b for _, b, _ in W]),
+                       np.stack([c for _, _, c in W]), S)
+    assert rel_err_rows(to_np(y), ref).max() <= VALUE_TOL
