@@ -282,7 +282,8 @@ SMOE_API int smoe_layer_forward_host(const smoe_desc* desc, const smoe_layer_wei
  *   gamma, beta [d] fp32 (LayerNorm over d, biased variance, eps 1e-5);
  *   w_gate_next [E, d] dtype; logits_q, logits_s nullable [T, E] fp32;
  *   pred_idx, true_idx [T, K] int32; hits [1] uint64, overwritten;
- *   qs_out nullable [2, T, d] dtype: the q rows then the s rows (else kept in ws).     */
+ *   qs_out nullable [2, T, d] dtype: the q rows then the s rows (else kept in ws).
+ * Requires d <= 8192 (the LayerNorm holds a row in registers); else SMOE_ERR_SHAPE.  */
 SMOE_API int smoe_prefetch_predict(const smoe_desc* desc, const float* r, const float* d_l,
                                    const void* y, const float* gamma, const float* beta,
                                    const void* w_gate_next, float* logits_q, float* logits_s,

@@ -130,3 +130,11 @@ def test_newer_entry_points_validate_on_the_host(lib):
     # smoe_combine(desc, y_disp, pair_row, topk_w, y_shared, y_out, ws, ws_bytes, stream)
     assert lib.smoe_combine(D, 16, 16 + 4, 16, None, 16, 256, n, None) == -3
     assert lib.smoe_combine(D, 16, 16, 16, None, None, 256, n, None) == -1
+
+
+def test_prefetch_rejects_d_above_8192(lib):
+    d = base_desc(d=8200)
+    n = B.workspace_size(d)
+    rc = lib.smoe_prefetch_predict(ctypes.byref(d), 16, 16, 16, 16, 16, 16, None, None, 16, 16,
+                                   16, None, 256, n, None)
+    assert rc == -2 and b"8192" in lib.smoe_last_error()
