@@ -650,3 +650,61 @@ def test_expert_ffn_skewed_and_odd_sizes(T, E, K, S, d, F, skew):
                        np.stack([a for a, _, _ in W]), np.stack([b for _, b, _ in W]),
                        np.stack([c for _, _, c in W]), S)
     assert rel_err_rows(to_np(y), ref).max() <= VALUE_TOL
+
+
+@pytest.mark.parametrize("T,d,E,K,H,dt", [(200, 64, 512, 32, 1, "bf16"), (300, 8, 16, 16, 16, "f32"),
+                                          (64, 8192, 8, 2, 1, "bf16"), (1, 128, 8, 2, 1, "bf16")])
+def test_prefetch_predict_at_limits(T, d, E, K, H, dt):
+    """The prefetch predictor at E = 512 / K = 32, at d = 8 and d = 8192 (its largest
+    row), and for a single token: routes and hits bit-exact given the GPU's logits,
+    logits against the oracle's LayerNorm + gate."""
+    rng = np.random.default_rng(d + E)
+    tdt = torch.float32 if dt == "f32" else torch.bfloat16
+    r = torch.as_tensor(rng.standard_normal((T, d)).astype(np.float32), device="cuda")
+    d_l = torch.as_tensor((0.3 * rng.standard_normal(d)).astype(np.float32), device="cuda")
+    y = torch.as_tensor(rng.standard_normal((T, d)).astype(np.float32)).to(tdt).cuda()
+    gamma = torch.as_tensor((1 + 0.1 * rng.standard_normal(d)).astype(np.float32), device="cuda")
+    beta = torch.as_tensor((0.1 * rng.standard_normal(d)).astype(np.float32), device="cuda")
+    wgn = torch.as_tensor((rng.standard_normal((E, d)) / np.sqrt(d)).astype(np.float32)).to(tdt).cuda()
+    desc = smoe.make_desc(T, d, E, K, H, 64, 0, 2, 16, dt)
+    ws = smoe.workspace(desc)
+    lq, ls = f32(T, E), f32(T, E)
+    pi, ti = i32(T, K), i32(T, K)
+    hits = torch.empty(1, dtype=torch.int64, device="cuda")
+    smoe.smoe_prefetch_predict(desc, r, d_l, y, gamma, beta, wgn, pi, ti, hits, ws,
+                               logits_q=lq, logits_s=ls)
+    smoe.smoe_get_status(ws)
+    torch.cuda.synchronize()
+    Lq, Ls = to_np(lq), to_np(ls)
+    rp, rtru = O.topk_select(Lq, K, H), O.topk_select(Ls, K, H)
+    assert np.array_equal(to_np(pi), rp) and np.array_equal(to_np(ti), rtru)
+    assert int(to_np(hits)[0]) == O.hit_count(rp, rtru)
+    ref = O.prefetch_predict(to_np(r), to_np(d_l), to_np(y).astype(np.float64), to_np(gamma),
+                             to_np(beta), to_np(wgn).astype(np.float64), K, H)
+    assert rel_err_rows(Lq, ref["logits_q"]).max() <= VALUE_TOL
+    assert rel_err_rows(Ls, ref["logits_s"]).max() <= VALUE_TOL
+
+
+def test_moe_forward_routed_at_limits():
+    """Caller-given routes at E = 512, K = 32 with 8 shared experts."""
+    T, d, E, K, S, F = 300, 64, 512, 32, 8, 64
+    rng = np.random.default_rng(9)
+    def t(a):
+        return torch.as_tensor(np.asarray(a, np.float32)).to(torch.bfloat16).cuda().contiguous()
+    x = t(rng.standard_normal((T, d)))
+    w1 = t(rng.standard_normal((E + S, F, d)) / np.sqrt(d))
+    w3 = t(rng.standard_normal((E + S, F, d)) / np.sqrt(d))
+    w2 = t(rng.standard_normal((E + S, d, F)) / np.sqrt(F))
+    idx_n = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+    w_n = rng.random((T, K)).astype(np.float32)
+    desc = smoe.make_desc(T, d, E, K, 1, F, S, 2, 16, "bf16")
+    ws = smoe.workspace(desc)
+    y = torch.empty_like(x)
+    smoe.smoe_moe_forward_routed(desc, x, torch.as_tensor(idx_n, device="cuda"),
+                                 torch.as_tensor(w_n, device="cuda"), w1, w3, w2, y, ws)
+    smoe.smoe_get_status(ws)
+    torch.cuda.synchronize()
+    ref = O.moe_output(to_np(x).astype(np.float64), idx_n, w_n.astype(np.float64),
+                       to_np(w1).astype(np.float64), to_np(w3).astype(np.float64),
+                       to_np(w2).astype(np.float64), S)
+    assert rel_err_rows(to_np(y), ref).max() <= VALUE_TOL
