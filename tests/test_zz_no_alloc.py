@@ -72,3 +72,16 @@ def test_noalloc_rejects_too_many_tokens(smoe):
                                                  t.data_ptr(), None, None)
     assert rc == -2
     assert b"1048576" in smoe.lib().smoe_last_error()
+
+
+def test_noalloc_at_the_token_limit(smoe):
+    # T = 1048576 fills every one of the scratch's 4096 tiles, with P = 32 partitions
+    T, d, E, P, V = 1024 * 1024, 8, 64, 32, 5000
+    desc = smoe.make_desc(T, d, E, 2, 1, 64, 0, P, V, "bf16")
+    ws = smoe.workspace(desc)
+    ids, conf, emap, x = make_inputs(7, T, d, E, P, V)
+    ref, got = run_both(smoe, desc, ids, conf, emap, x, ws)
+    for r, g in zip(ref, got):
+        assert torch.equal(r, g)
+    off = ref[2].cpu().numpy()
+    assert off[0] == 0 and off[-1] == T and (np.diff(off) >= 0).all()
