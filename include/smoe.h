@@ -306,6 +306,13 @@ SMOE_API int smoe_moe_forward_routed(const smoe_desc* desc, const void* x,
  * the workspace status word, and clears it. */
 SMOE_API int smoe_get_status(void* ws, void* stream);
 
+/* Self-test of the device-side failure path (the pages have no counterpart): one
+ * kernel waits on an mbarrier that nothing arrives at; the wait is the bounded wait
+ * every kernel uses (2 s), so it gives up, records a device timeout in the status word
+ * of `ws` and returns. The context stays usable; the next smoe_get_status(ws) returns
+ * SMOE_ERR_DEVICE_TIMEOUT. ws: any workspace of at least 256 bytes, zeroed status word. */
+SMOE_API int smoe_selftest_device_timeout(void* ws, size_t ws_bytes, void* stream);
+
 /* Static description of a status code. */
 SMOE_API const char* smoe_status_string(int status);
 

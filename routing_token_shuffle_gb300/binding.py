@@ -68,6 +68,7 @@ SIGNATURES = {
                                              _P, _SZ, _P]),
     "smoe_moe_forward_routed": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "smoe_get_status": (ctypes.c_int, [_P, _P]),
+    "smoe_selftest_device_timeout": (ctypes.c_int, [_P, _SZ, _P]),
     "smoe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "smoe_last_error": (ctypes.c_char_p, []),
     "smoe_kernel_launches": (ctypes.c_ulonglong, []),
@@ -254,3 +255,8 @@ def kernel_launches() -> int:
 
 def smoe_get_status(ws, stream=None):
     _check(lib().smoe_get_status(_ptr(ws), _stream(stream)), "smoe_get_status")
+
+
+def smoe_selftest_device_timeout(ws, stream=None):
+    _check(lib().smoe_selftest_device_timeout(_ptr(ws), ws.numel(), _stream(stream)),
+           "smoe_selftest_device_timeout")

@@ -552,6 +552,17 @@ SMOE_API int smoe_prefetch_predict(const smoe_desc* desc, const float* r, const 
   return SMOE_OK;
 }
 
+SMOE_API int smoe_selftest_device_timeout(void* ws, size_t ws_bytes, void* stream) {
+  SMOE_REQUIRE(ws != nullptr, SMOE_ERR_ARG, "workspace must not be NULL");
+  SMOE_REQUIRE(aligned16(ws), SMOE_ERR_ALIGN, "workspace must be 16-byte aligned");
+  SMOE_REQUIRE(ws_bytes >= 256, SMOE_ERR_WORKSPACE, "workspace smaller than its status word");
+  SMOE_CHECK(check_device());
+  cudaError_t e = launch_timeout_probe(ws_ptr<DeviceStatus>(ws, 0),
+                                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "timeout probe launch");
+  return SMOE_OK;
+}
+
 SMOE_API int smoe_get_status(void* ws, void* stream) {
   SMOE_REQUIRE(ws != nullptr, SMOE_ERR_ARG, "workspace must not be NULL");
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -23,7 +23,7 @@ struct DeviceStatus {
 
 enum : int32_t {
   kBadTokenId = 1, kBadExpertPart = 2, kBadTopkIdx = 3, kBadPerm = 4, kBadPairRow = 5,
-  kBadSrcPart = 6, kTimeoutGemm = 16
+  kBadSrcPart = 6, kTimeoutGemm = 16, kTimeoutProbe = 17
 };
 
 __device__ __forceinline__ void record_error(DeviceStatus* st, uint32_t flag, int32_t kind,
@@ -155,6 +155,8 @@ inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_
   } while (0)
 
 // ---------------------------------------------------------------- launchers
+cudaError_t launch_timeout_probe(DeviceStatus* st, cudaStream_t s);
+
 // Each returns cudaSuccess or the launch error; shapes are validated by the caller.
 int route_splits(const smoe_desc& d, int rows);  // K splits of the tensor-core gate GEMM
 

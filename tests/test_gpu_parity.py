@@ -708,3 +708,21 @@ def test_moe_forward_routed_at_limits():
                        to_np(w1).astype(np.float64), to_np(w3).astype(np.float64),
                        to_np(w2).astype(np.float64), S)
     assert rel_err_rows(to_np(y), ref).max() <= VALUE_TOL
+
+
+def test_device_timeout_is_reported_and_the_context_survives():
+    """A bounded device wait that can never complete gives up after its limit, the
+    status word reports SMOE_ERR_DEVICE_TIMEOUT, and the next launches run normally."""
+    c = get_case("tiny_fp32", None)
+    cfg = c.cfg
+    desc = smoe.desc_from_config(cfg)
+    ws = smoe.workspace(desc)
+    smoe.smoe_selftest_device_timeout(ws)
+    with pytest.raises(smoe.SmoeError) as ei:
+        smoe.smoe_get_status(ws)
+    assert ei.value.code == -7
+    smoe.smoe_get_status(ws)                       # cleared
+    logits, idx, w = run_route(c, desc, ws)
+    smoe.smoe_get_status(ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_np(idx), O.topk_select(to_np(logits), cfg.K, cfg.H))
