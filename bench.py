@@ -56,11 +56,17 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
-def init_dist(world: int, backend: str):
+def init_dist(world: int, backend: str, timeout_s: float | None = None):
+    """Join the process group (world > 1). With timeout_s, a collective that a rank never
+    joins (it failed or exited) raises on the others after that many seconds instead of
+    blocking: the host-side failure detection of the multi-rank bench."""
+    import datetime
+
     import torch.distributed as dist
     if world > 1 and not dist.is_initialized():
         os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
-        dist.init_process_group(backend=backend)
+        kw = {} if timeout_s is None else {"timeout": datetime.timedelta(seconds=timeout_s)}
+        dist.init_process_group(backend=backend, **kw)
     return world > 1
 
 
@@ -306,9 +312,20 @@ class Workload:
     STAGES = ("route", "predict_shuffle", "lar", "dispatch", "expert_ffn", "combine", "prefetch")
 
     def step(self, events=None):
-        """One forward of the layer; records an event after each stage when given."""
+        """One forward of the layer; records an event after each stage when given. Each
+        stage is also an NVTX range (named as in STAGES) for timeline profilers."""
+        import torch
         s, c = self.smoe, self
-        rec = (lambda i: events[i].record()) if events is not None else (lambda i: None)
+        nvtx = torch.cuda.nvtx
+
+        def rec(i):
+            nvtx.range_pop()
+            if events is not None:
+                events[i].record()
+            if i + 1 < len(Workload.STAGES):
+                nvtx.range_push(Workload.STAGES[i + 1])
+
+        nvtx.range_push(Workload.STAGES[0])
         s.smoe_route(c.desc, c.x, c.w_gate, c.idx, c.w, logits_out=c.logits, ws=c.ws)
         rec(0)
         s.smoe_predict_shuffle(c.desc, c.ids_d, c.conf_d, c.emap_d, c.pred, c.perm, c.part_off,

@@ -726,3 +726,61 @@ def test_device_timeout_is_reported_and_the_context_survives():
     smoe.smoe_get_status(ws)
     torch.cuda.synchronize()
     assert np.array_equal(to_np(idx), O.topk_select(to_np(logits), cfg.K, cfg.H))
+
+
+@pytest.mark.parametrize("name,T", [("tiny_fp32", 37), ("dsv2_prefill", 1537), ("qwen3_foe", 3001)],
+                         ids=["tiny-T37", "dsv2-T1537", "qwen3-T3001"])
+def test_no_write_past_any_buffer(name, T):
+    """Canary words after every output buffer and after the workspace: a layer forward
+    (and the prefetch predictor on the Qwen3 shape) writes nothing past the sizes the
+    header documents."""
+    c = get_case(name, T)
+    cfg = c.cfg
+    desc = smoe.desc_from_config(cfg)
+    CAN = 4096                                   # bytes of canary after each buffer
+    MAGIC = 0x5A
+
+    def guarded(nbytes):
+        buf = torch.full((nbytes + CAN,), MAGIC, dtype=torch.uint8, device="cuda")
+        return buf
+
+    def view(buf, shape, dtype):
+        n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        return buf[:n].view(dtype).view(*shape)
+
+    ws_n = smoe.workspace_size(desc)
+    ws_buf = guarded(ws_n)
+    ws_buf[:256].zero_()
+    ws = ws_buf[:ws_n]
+    TK = cfg.T * cfg.K
+    i4, f4 = torch.int32, torch.float32
+    shapes = dict(logits=((cfg.T, cfg.E), f4), topk_idx=((cfg.T, cfg.K), i4),
+                  topk_w=((cfg.T, cfg.K), f4), pred_part=((cfg.T,), i4), shuf_perm=((cfg.T,), i4),
+                  part_off=((cfg.P + 1,), i4), expert_off=((cfg.E + 1,), i4),
+                  pair_row=((cfg.T, cfg.K), i4), row_token=((TK,), i4), lar=((4,), torch.int64))
+    bufs, outs = {}, {}
+    for k, (shape, dt) in shapes.items():
+        nbytes = int(np.prod(shape)) * torch.empty((), dtype=dt).element_size()
+        bufs[k] = guarded(nbytes)
+        outs[k] = view(bufs[k], shape, dt)
+    ybytes = cfg.T * cfg.d * c.x.element_size()
+    bufs["y"] = guarded(ybytes)
+    y = view(bufs["y"], (cfg.T, cfg.d), c.x.dtype)
+    W = smoe.layer_weights(c.w_gate, c.w1, c.w3, c.w2, c.conf_d, c.emap_d)
+    smoe.smoe_layer_forward(desc, W, smoe.layer_io(c.x, c.ids_d, y, **outs), ws)
+    if cfg.prefetch:
+        r, wgn, gamma, beta = synth.predictor_inputs(cfg, "cuda")
+        d_l = torch.zeros(cfg.d, device="cuda")
+        for k, shape in (("pi", (cfg.T, cfg.K)), ("ti", (cfg.T, cfg.K))):
+            bufs[k] = guarded(int(np.prod(shape)) * 4)
+            outs[k] = view(bufs[k], shape, i4)
+        bufs["hits"] = guarded(8)
+        hits = view(bufs["hits"], (1,), torch.int64)
+        smoe.smoe_prefetch_predict(desc, r, d_l, y, gamma, beta, wgn.to(cfg.torch_dtype),
+                                   outs["pi"], outs["ti"], hits, ws)
+    smoe.smoe_get_status(ws)
+    torch.cuda.synchronize()
+    for k, buf in bufs.items():
+        tail = buf[buf.numel() - CAN:]
+        assert bool((tail == MAGIC).all()), f"write past the end of {k}"
+    assert bool((ws_buf[ws_n:] == MAGIC).all()), "write past the end of the workspace"
