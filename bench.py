@@ -46,6 +46,10 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-placement", action="store_true",
                    help="skip the (untimed) co-clustered placement report")
+    p.add_argument("--tokens", type=int, default=None,
+                   help="override the workload's batch size T (the default is its own T)")
+    p.add_argument("--seed", type=int, default=0,
+                   help="draw another seeded token batch (weights and tables unchanged)")
     p.add_argument("--cpu-seconds", type=float, default=15.0,
                    help="target CPU time of the oracle baseline sample")
     return p.parse_args(argv)
@@ -202,7 +206,8 @@ class ClockSampler:
 class Workload:
     """Device-resident inputs of one workload and the per-stage C-ABI calls of a step."""
 
-    def __init__(self, name: str, device, rank: int = 0, prepare_with_oracle: bool = False):
+    def __init__(self, name: str, device, rank: int = 0, prepare_with_oracle: bool = False,
+                 tokens: int | None = None, seed: int = 0):
         import numpy as np
         import torch
 
@@ -211,11 +216,15 @@ class Workload:
 
         self.smoe = smoe
         cfg = synth.CONFIGS[name]
+        if tokens is not None:
+            import dataclasses
+            cfg = dataclasses.replace(cfg, T=tokens)
         self.cfg = cfg
         dev = torch.device(device)
         self.dev = dev
         self.emb = synth.Embedding(cfg, dev)
-        self.ids, x32 = synth.token_batch(cfg, self.emb, "ids", cfg.T, dev, salt=rank)
+        self.ids, x32 = synth.token_batch(cfg, self.emb, "ids", cfg.T, dev,
+                                          salt=rank + 1000 * seed)
         self.x = x32.to(cfg.torch_dtype).contiguous()
         del x32
         self.w_gate, self.w1, self.w3, self.w2 = synth.layer_weights_lowp(cfg, dev)
@@ -478,7 +487,7 @@ def run_native(args):
     active = init_dist(world, "nccl")
     barrier(active)
     build_mod.build()
-    wl = Workload(args.workload, dev, rank=rank)
+    wl = Workload(args.workload, dev, rank=rank, tokens=args.tokens, seed=args.seed)
     cfg = wl.cfg
     peaks, peaks_kind = load_peaks()
 
@@ -683,7 +692,8 @@ def run_reference(args):
         return
     import torch
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    wl = Workload(args.workload, dev, prepare_with_oracle=True)
+    wl = Workload(args.workload, dev, prepare_with_oracle=True, tokens=args.tokens,
+                  seed=args.seed)
     per_step = max(1.0, min(args.cpu_seconds, 150.0 / max(args.steps + args.warmup, 1)))
     rate, n, secs, cores = cpu_oracle_rate(wl, per_step)
     import oracle as O
