@@ -14,7 +14,8 @@
 // Selection: 8 or 16 lanes per token (one warp per token when E > 256 or K > 16), the
 // token's fp32 logits spread over those lanes; each pick is a butterfly argmax under the
 // total order (logit descending, expert index ascending), so equal logits (including
-// +0 / -0) go to the lower index.
+// +0 / -0) go to the lower index. Grouped top-1 over 8 groups (FoE with H = K = 8) has
+// its own static-index kernel.
 #include <algorithm>
 
 #include "tc_common.cuh"
@@ -193,6 +194,89 @@ select_sub_kernel(const float* __restrict__ part, int KS, long long split_stride
       if (bi < E && (bi & (L - 1)) == j) taken |= 1u << (bi / L);
       if (j == h * kh + q) { my_v = bv; my_i = bi; }
     }
+  }
+  float w = j < K ? expf(my_v - m) / sum : 0.0f;
+  if (renorm) {
+    float sw = w;
+#pragma unroll
+    for (int off = L >> 1; off; off >>= 1) sw += __shfl_xor_sync(0xffffffffu, sw, off);
+    w = w / sw;
+  }
+  if (valid && j < K) {
+    topk_idx[(size_t)to * K + j] = my_i;
+    topk_w[(size_t)to * K + j] = w;
+  }
+}
+
+// Grouped top-1 (K = H, one pick per group, as FoE's top-K/H = 1): with E = L * H * VPG,
+// lane j's values i in [h VPG, (h+1) VPG) are exactly its experts of group h, so each
+// group is one short local scan plus one butterfly, and every index is static. Same
+// picks, order and weights as select_sub_kernel (within a lane the expert index grows
+// with i, so strict > keeps the lower index; the butterfly breaks ties the same way).
+template <int L, int H_, int VPG>
+__global__ void __launch_bounds__(256)
+select_group1_kernel(const float* __restrict__ part, int KS, long long split_stride,
+                     float* __restrict__ logits_out, int T, int renorm,
+                     int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                     RouteSplitOut so) {
+  pdl_wait_and_trigger();
+  constexpr int kPer = H_ * VPG, E = L * kPer, K = H_;
+  const int j = threadIdx.x & (L - 1);
+  const int t = (int)((blockIdx.x * blockDim.x + threadIdx.x) / L);
+  const bool valid = t < T;  // every lane stays for the shuffles
+  const bool second = valid && t >= so.split;
+  const int to = second ? t - so.split : t;
+  if (second) {
+    logits_out = so.logits;
+    topk_idx = so.idx;
+    topk_w = so.w;
+  }
+  float v[kPer];
+  const float* prow = part + (size_t)(valid ? t : 0) * E + j;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) v[i] = valid ? prow[L * i] : -INFINITY;
+#pragma unroll 4
+  for (int s = 1; s < KS; ++s) {
+    const float* ps = prow + (size_t)s * split_stride;
+    float a[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) a[i] = valid ? ps[L * i] : 0.0f;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) v[i] += a[i];
+  }
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    if (valid && logits_out) logits_out[(size_t)to * E + j + L * i] = v[i];
+    m = fmaxf(m, v[i]);
+  }
+#pragma unroll
+  for (int off = L >> 1; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  float sum = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) sum += expf(v[i] - m);
+#pragma unroll
+  for (int off = L >> 1; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  float my_v = -INFINITY;
+  int my_i = 0;
+#pragma unroll
+  for (int h = 0; h < H_; ++h) {
+    float bv = v[h * VPG];
+    int bi = j + L * h * VPG;
+#pragma unroll
+    for (int u = 1; u < VPG; ++u) {
+      if (v[h * VPG + u] > bv) {
+        bv = v[h * VPG + u];
+        bi = j + L * (h * VPG + u);
+      }
+    }
+#pragma unroll
+    for (int off = L >> 1; off; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+    }
+    if (j == h) { my_v = bv; my_i = bi; }
   }
   float w = j < K ? expf(my_v - m) / sum : 0.0f;
   if (renorm) {
@@ -458,6 +542,19 @@ cudaError_t launch_route(const smoe_desc& d, int rows, const void* x, const void
   }
   float* lo = logits_out == logits_in ? nullptr : logits_out;
   const long long stride = (long long)rows * d.E;
+  if (d.H == 8 && d.K == 8 && (d.E == 64 || d.E == 128 || d.E == 256)) {
+    const int grid = ceil_div(rows * 8, 256);
+    if (d.E == 64)
+      SMOE_LAUNCH((select_group1_kernel<8, 8, 1>), grid, 256, 0, s, part, KS, stride, lo, rows,
+                  d.renorm, topk_idx, topk_w, so);
+    else if (d.E == 128)
+      SMOE_LAUNCH((select_group1_kernel<8, 8, 2>), grid, 256, 0, s, part, KS, stride, lo, rows,
+                  d.renorm, topk_idx, topk_w, so);
+    else
+      SMOE_LAUNCH((select_group1_kernel<8, 8, 4>), grid, 256, 0, s, part, KS, stride, lo, rows,
+                  d.renorm, topk_idx, topk_w, so);
+    return cudaGetLastError();
+  }
   if (d.K <= 8 && d.E <= 128) {
     const int grid = ceil_div(rows * 8, 256);
     if (d.E <= 32)

@@ -92,12 +92,13 @@ def test_route(name, T):
 @pytest.mark.parametrize("E,K,H", [(8, 2, 1), (160, 6, 1), (128, 8, 8), (64, 8, 2), (512, 32, 1),
                                    (16, 16, 16), (33 * 3, 3, 3), (8, 8, 1), (32, 8, 1),
                                    (33, 3, 1), (65, 5, 1), (129, 9, 1), (256, 16, 2),
-                                   (257, 4, 1), (300, 20, 5)])
+                                   (257, 4, 1), (300, 20, 5), (64, 8, 8), (256, 8, 8)])
 @pytest.mark.parametrize("renorm", [0, 1])
 def test_route_selection_ties(E, K, H, renorm):
     """Many exact ties (small-integer logits, +0 and -0): lower index wins. The shapes
     cover every selection kernel: 8 lanes per token (E <= 32, 64, 128), 16 lanes
-    (E <= 256 or 8 < K <= 16) and one warp per token (E > 256 or K > 16)."""
+    (E <= 256 or 8 < K <= 16), one warp per token (E > 256 or K > 16) and grouped top-1
+    over 8 groups (E = 64, 128, 256)."""
     T = 777
     rng = np.random.default_rng(E + K + H)
     vals = np.array([-2.0, -1.0, -0.0, 0.0, 1.0, 3.0], np.float32)
