@@ -140,6 +140,7 @@ struct Tile {
   int b_row;          // first B row
   long long out_row;  // first output row (in out, or in out_sh for a shared down tile)
   bool out_shared;
+  bool m128;          // two-SM tile of 128 rows (64 per CTA): a group's last <= 128 rows
 };
 
 template <bool UP>
@@ -368,12 +369,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 
 // ------------------------------------------------------------------ two-SM variant
 // A cluster of two CTAs (on the two SMs of a TPC) computes 256 x 256 tiles with
-// tcgen05.mma.cta_group::2: each CTA loads its own 128 rows of A and 128 rows of B
-// (up: the leader W1, the peer W3; down: each half of the 256 W2 rows), so each SM
-// receives 32 KB per 64-wide k-block instead of 48 KB for the same MMA rate. The
-// leader's thread issues the MMAs; stage bytes of both CTAs complete on the leader's
+// tcgen05.mma.cta_group::2: each CTA loads its own 128 rows of A and 128 rows of B, so
+// each SM receives 32 KB per 64-wide k-block instead of 48 KB for the same MMA rate.
+// B halves: up, 64 W1 rows then the same 64 W3 rows (leader: features n0 .. n0+63,
+// peer: n0+64 .. n0+127), so that every accumulator row holds the gate and the up value
+// of each of its features; down, the leader's and the peer's 128 of the 256 W2 rows.
+// A group whose last rows fit in 128 ends with an M = 128 tile: 64 A rows per CTA, and
+// the accumulator of a CTA holds its 64 rows x the first N/2 columns in lanes 0-63 and
+// x the last N/2 columns in lanes 64-127 (TMEM columns 0 .. N/2-1 in both cases).
+// The leader's thread issues the MMAs; stage bytes of both CTAs complete on the leader's
 // `full` barrier; MMA completion is multicast to both CTAs' `empty` and `tfull`; both
-// epilogues drain their own 128 TMEM lanes and arrive on the leader's `tempty`.
+// epilogues drain their own TMEM lanes and arrive on the leader's `tempty`.
 constexpr int kPairStages = 6;
 constexpr uint32_t kPairStage = 128 * 128;  // A half or B half: 128 rows x 128 bytes
 constexpr size_t kPairSmemBytes = 1024 + kPairStages * 2 * kPairStage + kStageOut + 256 +
@@ -392,16 +398,17 @@ __device__ __forceinline__ void decode_pair_tile(const int32_t* ts, const int32_
   const int mt = ts[g + 1] - ts[g];  // 256-row pairs of this group
   const int local = t - ts[g] * p.NT;
   const int n_tile = local / mt, m_pair = local - n_tile * mt;
-  r.g = g;
-  r.m0 = m_pair * 256 + (int)rank * 128;
   const bool shared = g >= p.E;
   const int j = g - p.E;
+  r.g = g;
   r.rows = shared ? p.T : eo[g + 1] - eo[g];
+  r.m128 = r.rows - m_pair * 256 <= 128;
+  r.m0 = m_pair * 256 + (int)rank * (r.m128 ? 64 : 128);
   if (UP) {
     r.n0 = n_tile * 128;
     r.a_shared = shared;
     r.a_row = (shared ? 0 : eo[g]) + r.m0;
-    r.b_row = g * p.N + r.n0;  // leader: W1 rows, peer: W3 rows
+    r.b_row = g * p.N + r.n0 + (int)rank * 64;  // W1 and W3 rows of this CTA's 64 features
     r.out_row = (long long)(shared ? p.TK + j * p.T : eo[g]) + r.m0;
     r.out_shared = false;
   } else {
@@ -416,13 +423,16 @@ __device__ __forceinline__ void decode_pair_tile(const int32_t* ts, const int32_
 
 template <bool UP>
 __global__ void __launch_bounds__(kThreads, 1)
-grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
-                         const __grid_constant__ CUtensorMap tmA_sh,
+grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,     // 128-row box
+                         const __grid_constant__ CUtensorMap tmA_sh,  // 128-row box
+                         const __grid_constant__ CUtensorMap tmA64,   // 64-row box
+                         const __grid_constant__ CUtensorMap tmA_sh64,
                          const __grid_constant__ CUtensorMap tmB1,
                          const __grid_constant__ CUtensorMap tmB3, const GemmArgs p) {
   pdl_wait_and_trigger();
   using TE = __nv_bfloat16;
   constexpr uint32_t kIdesc = tc::instr_desc(false, 256, 256);
+  constexpr uint32_t kIdesc128 = tc::instr_desc(false, 128, 256);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -457,6 +467,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
     tc::mbar_init_fence();
     tc::tma_prefetch_map(&tmA);
     tc::tma_prefetch_map(&tmA_sh);
+    tc::tma_prefetch_map(&tmA64);
+    tc::tma_prefetch_map(&tmA_sh64);
     tc::tma_prefetch_map(&tmB1);
     tc::tma_prefetch_map(&tmB3);
   }
@@ -477,20 +489,23 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
 
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------------- TMA producer
-    const CUtensorMap* bmap = (UP && rank == 1) ? &tmB3 : &tmB1;
     uint32_t it = 0;
     bool ok = true;
     for (int t = pair; t < total && ok; t += npairs) {
       Tile tl;
       decode_pair_tile<UP>(s_ts, s_eo, p, t, rank, tl);
-      const CUtensorMap* amap = tl.a_shared ? &tmA_sh : &tmA;
+      const CUtensorMap* amap = tl.m128 ? (tl.a_shared ? &tmA_sh64 : &tmA64)
+                                        : (tl.a_shared ? &tmA_sh : &tmA);
+      const uint32_t tx = 2 * ((tl.m128 ? kPairStage / 2 : kPairStage) + kPairStage);
       for (int kb = 0; kb < nkb; ++kb, ++it) {
         const uint32_t s = it % kPairStages, ph = (it / kPairStages) & 1u;
         if (!tc::mbar_wait(&empty[s], ph ^ 1u, abort)) { ok = false; break; }
         const uint32_t leader_full = tc::cluster_addr(&full[s], 0);
-        if (rank == 0) tc::mbar_expect_tx(&full[s], 4 * kPairStage);
+        if (rank == 0) tc::mbar_expect_tx(&full[s], tx);
+        uint8_t* b = sB + s * kPairStage;
         tc::tma_load_2d_pair(sA + s * kPairStage, amap, leader_full, kb * 64, tl.a_row);
-        tc::tma_load_2d_pair(sB + s * kPairStage, bmap, leader_full, kb * 64, tl.b_row);
+        tc::tma_load_2d_pair(b, &tmB1, leader_full, kb * 64, tl.b_row);
+        if (UP) tc::tma_load_2d_pair(b + kPairStage / 2, &tmB3, leader_full, kb * 64, tl.b_row);
       }
     }
     if (!ok) {
@@ -502,6 +517,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
     uint32_t it = 0, tcount = 0;
     bool ok = true;
     for (int t = pair; t < total && ok; t += npairs, ++tcount) {
+      Tile tl;
+      decode_pair_tile<UP>(s_ts, s_eo, p, t, rank, tl);
+      const uint32_t idesc = tl.m128 ? kIdesc128 : kIdesc;
       const uint32_t a = tcount & 1u, aph = (tcount >> 1) & 1u;
       if (!tc::mbar_wait(&tempty[a], aph ^ 1u, abort)) { ok = false; break; }
       tc::fence_after_sync();
@@ -514,7 +532,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         const uint64_t bdesc = tc::sw128_kmajor_desc(tc::smem_u32(sB + s * kPairStage));
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          tc::mma_bf16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, kIdesc,
+          tc::mma_bf16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc,
                             (kb > 0 || k > 0) ? 1u : 0u);
         tc::commit_pair(&empty[s], 0x3);
       }
@@ -542,37 +560,48 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         break;
       }
       tc::fence_after_sync();
+      // This warp's TMEM lanes: for M = 256, rows 32q .. 32q+31 of the CTA's 128 over all
+      // N columns; for M = 128, rows 32 (q & 1) .. of the CTA's 64 over the N columns of
+      // half (q >> 1), in TMEM columns 0 .. 127.
+      const int rsub = tl.m128 ? (q & 1) : q;
+      const int nhalf = tl.m128 ? (q >> 1) : 0;
+      const int ncols = tl.m128 ? 128 : 256;
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + a * kAccCols;
       const RowStager<TE> rs{sOut + q * 4096, static_cast<TE*>(tl.out_shared ? p.out_sh : p.out),
-                             tl.out_row + q * 32, clamp_rows(tl.rows - tl.m0 - q * 32), p.N};
+                             tl.out_row + rsub * 32, clamp_rows(tl.rows - tl.m0 - rsub * 32),
+                             p.N};
       constexpr int kWin = RowStager<TE>::kColsPerFlush;
       if (UP) {
+        // each 128-column block: the gate of 64 features, then the up of the same features
 #pragma unroll 1
-        for (int c = 0; c < 128; c += 32) {
-          uint32_t gv[32], uv[32];
-          tc::tmem_ld32(taddr + c, gv);
-          tc::tmem_ld32(taddr + 128 + c, uv);
-          tc::tmem_ld_wait();
-          if (c == 96) {  // the accumulator is read out: the next tile's MMAs may start
-            tc::fence_before_sync();
-            tc::mbar_arrive_cluster(tc::cluster_addr(&tempty[a], 0));
-          }
-          float h[32];
+        for (int c0 = 0; c0 < ncols; c0 += 128) {
+#pragma unroll 1
+          for (int c = 0; c < 64; c += 32) {
+            uint32_t gv[32], uv[32];
+            tc::tmem_ld32(taddr + c0 + c, gv);
+            tc::tmem_ld32(taddr + c0 + 64 + c, uv);
+            tc::tmem_ld_wait();
+            if (c0 + 128 == ncols && c == 32) {  // read out: the next tile's MMAs may start
+              tc::fence_before_sync();
+              tc::mbar_arrive_cluster(tc::cluster_addr(&tempty[a], 0));
+            }
+            float h[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float gg = __uint_as_float(gv[i]);
-            h[i] = gg / (1.0f + __expf(-gg)) * __uint_as_float(uv[i]);
+            for (int i = 0; i < 32; ++i) {
+              const float gg = __uint_as_float(gv[i]);
+              h[i] = gg / (1.0f + __expf(-gg)) * __uint_as_float(uv[i]);
+            }
+            rs.put32(lane, c, h);
           }
-          rs.put32(lane, c, h);
-          if ((c + 32) % kWin == 0) rs.flush(lane, tl.n0 + c + 32 - kWin);
+          rs.flush(lane, tl.n0 + 64 * nhalf + c0 / 2);
         }
       } else {
 #pragma unroll 1
-        for (int c = 0; c < 256; c += 32) {
+        for (int c = 0; c < ncols; c += 32) {
           uint32_t yv[32];
           tc::tmem_ld32(taddr + c, yv);
           tc::tmem_ld_wait();
-          if (c == 224) {
+          if (c + 32 == ncols) {
             tc::fence_before_sync();
             tc::mbar_arrive_cluster(tc::cluster_addr(&tempty[a], 0));
           }
@@ -580,7 +609,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
           for (int i = 0; i < 32; ++i) y[i] = __uint_as_float(yv[i]);
           rs.put32(lane, c, y);
-          if ((c + 32) % kWin == 0) rs.flush(lane, tl.n0 + c + 32 - kWin);
+          if ((c + 32) % kWin == 0) rs.flush(lane, tl.n0 + 128 * nhalf + c + 32 - kWin);
         }
       }
     }
@@ -593,7 +622,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
 }
 
 template <bool UP>
-cudaError_t launch_gemm_pair(const CUtensorMap& A, const CUtensorMap& Ash, const CUtensorMap& B1,
+cudaError_t launch_gemm_pair(const CUtensorMap& A, const CUtensorMap& Ash, const CUtensorMap& A64,
+                             const CUtensorMap& Ash64, const CUtensorMap& B1,
                              const CUtensorMap& B3, const GemmArgs& args, long long tile_bound,
                              cudaStream_t s);
 
@@ -618,7 +648,8 @@ cudaError_t launch_gemm(const CUtensorMap& A, const CUtensorMap& Ash, const CUte
 }
 
 template <bool UP>
-cudaError_t launch_gemm_pair(const CUtensorMap& A, const CUtensorMap& Ash, const CUtensorMap& B1,
+cudaError_t launch_gemm_pair(const CUtensorMap& A, const CUtensorMap& Ash, const CUtensorMap& A64,
+                             const CUtensorMap& Ash64, const CUtensorMap& B1,
                              const CUtensorMap& B3, const GemmArgs& args, long long tile_bound,
                              cudaStream_t s) {
   auto kern = grouped_gemm_pair_kernel<UP>;
@@ -641,13 +672,16 @@ cudaError_t launch_gemm_pair(const CUtensorMap& A, const CUtensorMap& Ash, const
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   SMOE_COUNT_LAUNCH(1);
-  return cudaLaunchKernelEx(&cfg, kern, A, Ash, B1, B3, args);
+  return cudaLaunchKernelEx(&cfg, kern, A, Ash, A64, Ash64, B1, B3, args);
 }
 
-// Two-SM tiles pay off when experts hold enough rows that a 256-row tile is rarely
-// mostly padding.
+// Two-SM tiles (with M = 128 tiles for a group's last <= 128 rows) pad like single-SM
+// tiles and move less data per SM; below about 256 rows per expert the FFN streams
+// weights and the single-SM tiles, with twice as many CTAs issuing loads, keep more
+// bytes in flight.
+constexpr int kPairMinRows = 256;
 bool use_pair_tiles(const smoe_desc& d) {
-  return d.dtype == SMOE_BF16 && (long long)d.T * d.K >= 512LL * d.E;
+  return d.dtype == SMOE_BF16 && (long long)d.T * d.K >= (long long)kPairMinRows * d.E;
 }
 
 template <bool F32>
@@ -667,30 +701,51 @@ cudaError_t run_ffn(const smoe_desc& d, const void* x_disp, const void* x,
 
   const long long mtile_bound =
       ceil_div(TK, bm) + d.E + (long long)d.n_shared * ceil_div(d.T, bm);
+  const uint64_t x_rows = d.n_shared ? d.T : TK;
+  const void* x_src = d.n_shared ? x : x_disp;
+  const uint64_t h_rows = (uint64_t)TK + (uint64_t)d.n_shared * d.T;
+  GemmArgs up{expert_off, tiles, hbuf, nullptr, st, d.E, G, d.T, TK, d.F, d.d, ceil_div(d.F, 128)};
+  GemmArgs dn{expert_off, tiles, y_disp, y_sh, st, d.E, G, d.T, TK, d.d, d.F, ceil_div(d.d, 256)};
+
+  if (pairs) {
+    // up: A = x_disp [TK, d] (shared experts: x [T, d]) in 128- and 64-row boxes;
+    // B = W1, W3 [(E+S) F, d] in 64-row boxes
+    alignas(64) CUtensorMap tA, tAsh, tA64, tAsh64, tB1, tB3;
+    if (!encode_tmap_2d(&tA, x_disp, false, TK, d.d, 128, 64) ||
+        !encode_tmap_2d(&tAsh, x_src, false, x_rows, d.d, 128, 64) ||
+        !encode_tmap_2d(&tA64, x_disp, false, TK, d.d, 64, 64) ||
+        !encode_tmap_2d(&tAsh64, x_src, false, x_rows, d.d, 64, 64) ||
+        !encode_tmap_2d(&tB1, w1, false, (uint64_t)G * d.F, d.d, 64, 64) ||
+        !encode_tmap_2d(&tB3, w3, false, (uint64_t)G * d.F, d.d, 64, 64))
+      return cudaErrorInvalidValue;
+    cudaError_t e =
+        launch_gemm_pair<true>(tA, tAsh, tA64, tAsh64, tB1, tB3, up, mtile_bound * up.NT, s);
+    if (e != cudaSuccess) return e;
+    // down: A = H [TK + S T, F]; B = W2 [(E+S) d, F] in 128-row boxes
+    alignas(64) CUtensorMap dA, dA64, dB;
+    if (!encode_tmap_2d(&dA, hbuf, false, h_rows, d.F, 128, 64) ||
+        !encode_tmap_2d(&dA64, hbuf, false, h_rows, d.F, 64, 64) ||
+        !encode_tmap_2d(&dB, w2, false, (uint64_t)G * d.d, d.F, 128, 64))
+      return cudaErrorInvalidValue;
+    return launch_gemm_pair<false>(dA, dA, dA64, dA64, dB, dB, dn, mtile_bound * dn.NT, s);
+  }
+
   alignas(64) CUtensorMap tA, tAsh, tB1, tB3;
   // up: A = x_disp [TK, d] (shared experts: x [T, d]); B = W1, W3 [(E+S) F, d]
-  if (!encode_tmap_2d(&tA, x_disp, F32, TK, d.d, kBM, box_k)) return cudaErrorInvalidValue;
-  if (!encode_tmap_2d(&tAsh, d.n_shared ? x : x_disp, F32, d.n_shared ? d.T : TK, d.d, kBM,
-                      box_k))
+  if (!encode_tmap_2d(&tA, x_disp, F32, TK, d.d, kBM, box_k) ||
+      !encode_tmap_2d(&tAsh, x_src, F32, x_rows, d.d, kBM, box_k) ||
+      !encode_tmap_2d(&tB1, w1, F32, (uint64_t)G * d.F, d.d, 128, box_k) ||
+      !encode_tmap_2d(&tB3, w3, F32, (uint64_t)G * d.F, d.d, 128, box_k))
     return cudaErrorInvalidValue;
-  if (!encode_tmap_2d(&tB1, w1, F32, (uint64_t)G * d.F, d.d, 128, box_k))
-    return cudaErrorInvalidValue;
-  if (!encode_tmap_2d(&tB3, w3, F32, (uint64_t)G * d.F, d.d, 128, box_k))
-    return cudaErrorInvalidValue;
-  GemmArgs up{expert_off, tiles, hbuf, nullptr, st, d.E, G, d.T, TK, d.F, d.d, ceil_div(d.F, 128)};
-  cudaError_t e = pairs ? launch_gemm_pair<true>(tA, tAsh, tB1, tB3, up, mtile_bound * up.NT, s)
-                        : launch_gemm<true, F32>(tA, tAsh, tB1, tB3, up, mtile_bound * up.NT, s);
+  cudaError_t e = launch_gemm<true, F32>(tA, tAsh, tB1, tB3, up, mtile_bound * up.NT, s);
   if (e != cudaSuccess) return e;
 
   // down: A = H [TK + S T, F]; B = W2 [(E+S) d, F]
   alignas(64) CUtensorMap dA, dB;
-  if (!encode_tmap_2d(&dA, hbuf, F32, (uint64_t)TK + (uint64_t)d.n_shared * d.T, d.F, kBM, box_k))
+  if (!encode_tmap_2d(&dA, hbuf, F32, h_rows, d.F, kBM, box_k) ||
+      !encode_tmap_2d(&dB, w2, F32, (uint64_t)G * d.d, d.F, 256, box_k))
     return cudaErrorInvalidValue;
-  if (!encode_tmap_2d(&dB, w2, F32, (uint64_t)G * d.d, d.F, pairs ? 128 : 256, box_k))
-    return cudaErrorInvalidValue;
-  GemmArgs dn{expert_off, tiles, y_disp, y_sh, st, d.E, G, d.T, TK, d.d, d.F, ceil_div(d.d, 256)};
-  return pairs ? launch_gemm_pair<false>(dA, dA, dB, dB, dn, mtile_bound * dn.NT, s)
-               : launch_gemm<false, F32>(dA, dA, dB, dB, dn, mtile_bound * dn.NT, s);
+  return launch_gemm<false, F32>(dA, dA, dB, dB, dn, mtile_bound * dn.NT, s);
 }
 
 // ------------------------------------------------------------------ tensor maps

@@ -414,9 +414,9 @@ def test_empty_batch():
 @pytest.mark.parametrize("T,E,K,S,d,F", [(2500, 8, 2, 0, 256, 384), (1537, 4, 2, 1, 512, 256),
                                          (4099, 16, 2, 0, 128, 640)])
 def test_expert_ffn_two_sm_tiles_ragged(T, E, K, S, d, F):
-    """Shapes with at least 512 rows per expert take the two-SM (256-row) tiles; ragged
-    expert segments, a partial last n-tile (F = 640, 384) and a shared expert."""
-    assert T * K >= 512 * E
+    """Shapes with at least 256 rows per expert take the two-SM tiles; ragged expert
+    segments, a partial last n-tile (F = 640, 384) and a shared expert."""
+    assert T * K >= 256 * E
     g = torch.Generator(device="cuda").manual_seed(T + E)
     x = (torch.randn(T, d, generator=g, device="cuda")).to(torch.bfloat16)
     w1 = (torch.randn(E + S, F, d, generator=g, device="cuda") / d ** 0.5).to(torch.bfloat16)
@@ -445,6 +445,43 @@ def test_expert_ffn_two_sm_tiles_ragged(T, E, K, S, d, F):
     assert rel_err_rows(to_np(yd), ref).max() <= VALUE_TOL
     for j in range(S):
         assert rel_err_rows(to_np(ysh[j]), O.swiglu_ffn(xn, *W[E + j])).max() <= VALUE_TOL
+
+
+@pytest.mark.parametrize("d,F", [(384, 704), (256, 256)])
+def test_expert_ffn_two_sm_tail_tiles(d, F):
+    """Two-SM tiles end a group with an M = 128 tile (64 rows per CTA) when its last rows
+    fit in 128 and with a full 256-row tile otherwise. Expert segments of 64, 300, 450, 0,
+    129, 128, 513 and 257 rows hit every case (a group that is only an M = 128 tile, M =
+    128 tails of 44, 1 and 1 rows, a 194-row M = 256 tail, a 129-row group, an empty
+    group), and the shared expert's 1100 rows end in a 76-row M = 128 tail; F = 704 and
+    d = 384 leave half-valid last n-tiles in the up and the down GEMM."""
+    counts = [64, 300, 450, 0, 129, 128, 513, 257]
+    E, K, S, T = len(counts), 2, 1, 1100
+    assert T * K >= 256 * E and sum(counts) <= T * K
+    g = torch.Generator(device="cuda").manual_seed(d + F)
+    x = torch.randn(T, d, generator=g, device="cuda").to(torch.bfloat16)
+    xd = torch.randn(T * K, d, generator=g, device="cuda").to(torch.bfloat16)
+    w1 = (torch.randn(E + S, F, d, generator=g, device="cuda") / d ** 0.5).to(torch.bfloat16)
+    w3 = (torch.randn(E + S, F, d, generator=g, device="cuda") / d ** 0.5).to(torch.bfloat16)
+    w2 = (torch.randn(E + S, d, F, generator=g, device="cuda") / F ** 0.5).to(torch.bfloat16)
+    eo_n = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    eo = torch.as_tensor(eo_n, device="cuda")
+    desc = smoe.make_desc(T, d, E, K, 1, F, S, 2, 100, "bf16")
+    ws = smoe.workspace(desc)
+    yd = torch.full_like(xd, 7.0)
+    ysh = torch.empty(S, T, d, dtype=torch.bfloat16, device="cuda")
+    smoe.smoe_expert_ffn(desc, xd, eo, w1, w3, w2, yd, ws, x=x, y_shared=ysh)
+    smoe.smoe_get_status(ws)
+    torch.cuda.synchronize()
+    xdn, xn = to_np(xd).astype(np.float64), to_np(x).astype(np.float64)
+    W = [tuple(to_np(m[e]).astype(np.float64) for m in (w1, w3, w2)) for e in range(E + S)]
+    y = to_np(yd)
+    for e in range(E):
+        lo, hi = eo_n[e], eo_n[e + 1]
+        if hi > lo:
+            assert rel_err_rows(y[lo:hi], O.swiglu_ffn(xdn[lo:hi], *W[e])).max() <= VALUE_TOL, e
+    assert (y[eo_n[-1]:] == 7.0).all()   # rows past the last group are not written
+    assert rel_err_rows(to_np(ysh[0]), O.swiglu_ffn(xn, *W[E])).max() <= VALUE_TOL
 
 
 @pytest.mark.parametrize("name,T", [("tiny_fp32", None), ("dsv2_prefill", 1537), ("qwen3_foe", 3001),
