@@ -114,6 +114,41 @@ def test_route_selection_ties(E, K, H, renorm):
                                atol=1e-7)
 
 
+
+@pytest.mark.parametrize("T,d,E,K,H", [(1001, 256, 8, 2, 1), (777, 512, 160, 6, 1),
+                                       (5000, 256, 128, 8, 8), (19000, 128, 64, 8, 2),
+                                       (300, 192, 16, 8, 8), (300, 192, 16, 16, 16),
+                                       (650, 320, 99, 3, 3),
+                                       (64, 1024, 8, 8, 1), (2000, 256, 256, 16, 2),
+                                       (129, 512, 256, 8, 8), (700, 256, 64, 8, 8),
+                                       (64, 5120, 160, 6, 1)])
+@pytest.mark.parametrize("renorm", [0, 1])
+def test_route_fused_gemm_ties(T, d, E, K, H, renorm):
+    """The bf16 gate GEMM with the selection in its epilogue (E <= 256, K <= 8 lanes per
+    token for E <= 128, else 16, at most one 128-row tile per SM), split over clusters of
+    1, 2, 4 or 8 CTAs; E = 16 with K = 16 takes the two-launch path. x and W_g in {-1, 0, 1} make every logit an exact
+    small integer, so the exported logits must equal the exact products and many of them
+    tie (the lower index must win); picks and weights are then checked against the
+    oracle's selection on those logits."""
+    rng = np.random.default_rng(T + d + E + K + H)
+    xn = rng.integers(-1, 2, size=(T, d)).astype(np.float32)
+    wn = rng.integers(-1, 2, size=(E, d)).astype(np.float32)
+    x = torch.as_tensor(xn, device="cuda").to(torch.bfloat16)
+    wg = torch.as_tensor(wn, device="cuda").to(torch.bfloat16)
+    desc = smoe.make_desc(T, d, E, K, H, 64, 0, 2, 100, "bf16", renorm)
+    ws = smoe.workspace(desc)
+    logits, idx, w = f32(T, E), i32(T, K), f32(T, K)
+    smoe.smoe_route(desc, x, wg, idx, w, logits_out=logits, ws=ws)
+    smoe.smoe_get_status(ws)
+    torch.cuda.synchronize()
+    L = to_np(logits)
+    exact = (xn.astype(np.float64) @ wn.astype(np.float64).T).astype(np.float32)
+    assert np.array_equal(L, exact)
+    ref = O.topk_select(L, K, H)
+    assert np.array_equal(to_np(idx), ref)
+    np.testing.assert_allclose(to_np(w), O.gate_weights(L, ref, renorm=bool(renorm)), rtol=2e-6,
+                               atol=1e-7)
+
 def run_shuffle(c, desc, ws, with_x=True):
     cfg = c.cfg
     pred, perm, off = i32(cfg.T), i32(cfg.T), i32(cfg.P + 1)
