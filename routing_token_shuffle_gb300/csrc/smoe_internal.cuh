@@ -92,7 +92,11 @@ struct WsLayout {
   size_t total;
 };
 
-constexpr int kSortTile = 1024;     // pairs per tile of the dispatch counting sort
+constexpr int kSortTile = 1024;     // largest tile (pairs) of the dispatch counting sort
+// Tile of the dispatch counting sort for this layer (256, 512 or 1024 pairs): halved from
+// 1024 while the tiles still fit two waves of a 152-SM GPU and the (expert, tile) table
+// stays within four rounds of the scan, so that small batches spread over more SMs.
+int dispatch_sort_tile(const smoe_desc& d);
 constexpr int kShufTile = 256;      // tokens per tile of the shuffle counting sort
 constexpr int kMaxGroups = 520;     // E + n_shared upper bound
 

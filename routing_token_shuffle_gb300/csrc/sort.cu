@@ -186,15 +186,15 @@ size_t predict_smem(int E) { return sizeof(float) * kPredTokens * E; }
 __global__ void __launch_bounds__(kThreads)
 dispatch_hist_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ perm, int T,
                      int K, int E, int32_t* __restrict__ bucket, int32_t* __restrict__ hist,
-                     int ntiles, DeviceStatus* st) {
+                     int ntiles, int tile, DeviceStatus* st) {
   pdl_wait_and_trigger();
   __shared__ int s_cnt[kMaxBuckets];
   const int tid = threadIdx.x;
   for (int b = tid; b < E; b += kThreads) s_cnt[b] = 0;
   __syncthreads();
   const long long n = (long long)T * K;
-  const long long q0 = (long long)blockIdx.x * kSortTile;
-  const long long q1 = min(q0 + kSortTile, n);
+  const long long q0 = (long long)blockIdx.x * tile;
+  const long long q1 = min(q0 + tile, n);
 #pragma unroll 4
   for (long long q = q0 + tid; q < q1; q += kThreads) {
     const int s = (int)(q / K), k = (int)(q - (long long)s * K);
@@ -485,6 +485,19 @@ int grid_for_rows(long long nrows) {
 }  // namespace
 
 // ------------------------------------------------------------------ launchers
+int dispatch_sort_tile(const smoe_desc& d) {
+  constexpr long long kWaveTiles = 2 * 152;   // two waves of a GB300's SMs
+  constexpr long long kMaxTable = 4 * 4096;   // four scan rounds
+  const long long n = (long long)d.T * d.K;
+  int tile = kSortTile;
+  while (tile > 256) {
+    const long long nt = (n + tile / 2 - 1) / (tile / 2);
+    if (nt > kWaveTiles || nt * d.E > kMaxTable) break;
+    tile /= 2;
+  }
+  return tile;
+}
+
 cudaError_t launch_predict_shuffle(const smoe_desc& d, const int32_t* ids, const float* conf,
                                    const int32_t* emap, const void* x, int32_t* pred,
                                    int32_t* perm, int32_t* part_off, void* x_shuf, void* ws,
@@ -537,12 +550,13 @@ cudaError_t launch_dispatch(const smoe_desc& d, const int32_t* idx, const int32_
   // per-pair buckets live in the second half of the workspace's row-source region
   int32_t* bucket = ws_rows + (size_t)d.T * d.K;
   const int n = d.T * d.K;
-  const int ntiles = ceil_div(n, kSortTile);
+  const int tile = dispatch_sort_tile(d);
+  const int ntiles = ceil_div(n, tile);
   SMOE_LAUNCH(dispatch_hist_kernel, ntiles, kThreads, 0, s, idx, perm, d.T, d.K, d.E, bucket, hist,
-      ntiles, st);
+      ntiles, tile, st);
   SMOE_LAUNCH(scan_kernel, 1, 1024, 0, s, hist, offs, d.E * ntiles, d.E, ntiles, n, expert_off);
-  SMOE_LAUNCH(scatter_kernel<kDispatch>, ntiles, kThreads, 0, s, bucket, n, d.E, ntiles,
-      kSortTile, offs, nullptr, perm, d.T, d.K, pair_row, row_token, row_src);
+  SMOE_LAUNCH(scatter_kernel<kDispatch>, ntiles, kThreads, 0, s, bucket, n, d.E, ntiles, tile,
+      offs, nullptr, perm, d.T, d.K, pair_row, row_token, row_src);
   if (x_disp) {
     const int vec = (int)(d.d * elem_size(d) / 16);
     SMOE_LAUNCH(gather_rows_kernel, grid_for_rows(n), kThreads, 0, s,
