@@ -121,7 +121,7 @@ bool ws_layout(const smoe_desc& d, WsLayout* L) {
   const size_t T = (size_t)d.T, K = (size_t)d.K, E = (size_t)d.E, P = (size_t)d.P;
   const size_t b = elem_size(d), dm = (size_t)d.d, F = (size_t)d.F, S = (size_t)d.n_shared;
   const size_t tile = (size_t)dispatch_sort_tile(d);
-  const size_t ntT = (T + kShufTile - 1) / kShufTile, ntTK = (T * K + tile - 1) / tile;
+  const size_t ntT = (T + kShufHistTokens - 1) / kShufHistTokens, ntTK = (T * K + tile - 1) / tile;
   const size_t hist_n = std::max(P * ntT, E * ntTK) + 1;
   L->status = take(256);
   L->sort_hist = take(4 * hist_n);

@@ -97,7 +97,8 @@ constexpr int kSortTile = 1024;     // largest tile (pairs) of the dispatch coun
 // 1024 while the tiles still fit two waves of a 152-SM GPU and the (expert, tile) table
 // stays within four rounds of the scan, so that small batches spread over more SMs.
 int dispatch_sort_tile(const smoe_desc& d);
-constexpr int kShufTile = 256;      // tokens per tile of the shuffle counting sort
+constexpr int kShufTile = 256;      // tokens per tile of the workspace-free shuffle's sort
+constexpr int kShufHistTokens = 32; // tokens per histogram column of the shuffle sort
 constexpr int kMaxGroups = 520;     // E + n_shared upper bound
 
 bool ws_layout(const smoe_desc& d, WsLayout* out);

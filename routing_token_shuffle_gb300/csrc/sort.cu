@@ -8,8 +8,10 @@
 //
 // A counting sort is three launches with no inter-CTA waiting: per-tile bucket
 // histograms, one CTA scanning the (bucket, tile) table, and a scatter that ranks
-// each tile's elements stably (warp match + per-warp counts in shared memory). Tiles
-// are 256 tokens for the shuffle and 1024 (token, expert) pairs for the dispatch.
+// each tile's elements stably (warp match + per-warp counts in shared memory). The
+// shuffle's histogram columns are the predict kernel's 32-token CTAs (written
+// directly, nothing to clear) and its scatter tiles 64 tokens; the dispatch's tiles are
+// 256 to 1024 (token, expert) pairs, chosen per layer.
 #include <algorithm>
 #include <mutex>
 
@@ -37,7 +39,8 @@ __device__ __forceinline__ unsigned lanemask_lt() {
 // order), and a butterfly argmax over the token's lanes with the order (score
 // descending, partition ascending) picks pred[t]. The CTA's partition counts are added
 // to its tile's histogram entries (which the launcher zeroes first).
-constexpr int kPredTokens = 32;
+constexpr int kPredTokens = kShufHistTokens;
+constexpr int kShufScatter = 64;  // tokens per scatter CTA of the shuffle
 
 // INTER: the inter-layer source of "Speculative MoE" §4.1 also votes. prev[t] is the
 // token's cluster at the previous layer and table_a [P, P] the 2-gram table A; A's row
@@ -48,7 +51,7 @@ __global__ void __launch_bounds__(kThreads)
 predict_hist_kernel(const int32_t* __restrict__ ids, const float* __restrict__ conf,
                     const int32_t* __restrict__ emap, int T, int E, int P, int vocab,
                     int32_t* __restrict__ pred, int32_t* __restrict__ hist, int ntiles,
-                    DeviceStatus* st, const int32_t* __restrict__ prev,
+                    int tile, DeviceStatus* st, const int32_t* __restrict__ prev,
                     const float* __restrict__ table_a, int K) {
   pdl_wait_and_trigger();
   extern __shared__ float s_rows[];          // [kPredTokens, E]
@@ -176,7 +179,13 @@ predict_hist_kernel(const int32_t* __restrict__ ids, const float* __restrict__ c
     }
   }
   __syncthreads();
-  if (tid < P && s_cnt[tid] > 0) atomicAdd(&hist[tid * ntiles + t0 / kShufTile], s_cnt[tid]);
+  // tile == kPredTokens: this CTA's counts are its own histogram column (no zeroing
+  // needed); larger tiles: added into the tile's column, which the launcher zeroes
+  if (tile == kPredTokens) {
+    if (tid < P) hist[tid * ntiles + blockIdx.x] = s_cnt[tid];
+  } else if (tid < P && s_cnt[tid] > 0) {
+    atomicAdd(&hist[tid * ntiles + t0 / tile], s_cnt[tid]);
+  }
 }
 
 size_t predict_smem(int E) { return sizeof(float) * kPredTokens * E; }
@@ -274,13 +283,15 @@ scan_kernel(const int32_t* __restrict__ hist, int32_t* __restrict__ offs, int L,
 // ------------------------------------------------------------------ scatter
 // Stable rank of every element of a tile within its bucket: chunks of kThreads
 // elements in index order; inside a chunk, warps in order, inside a warp, lanes in
-// order (warp match gives the peers of equal bucket).
+// order (warp match gives the peers of equal bucket). A scatter tile may span
+// col_stride consecutive histogram columns: its running start per bucket is the scanned
+// offset of its first column.
 enum ScatterMode { kShuffle = 0, kDispatch = 1 };
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads)
 scatter_kernel(const int32_t* __restrict__ bucket, int n, int B, int ntiles, int tile,
-               const int32_t* __restrict__ offs,
+               int col_stride, const int32_t* __restrict__ offs,
                // kShuffle: perm_out[pos] = i
                int32_t* __restrict__ perm_out,
                // kDispatch
@@ -291,7 +302,7 @@ scatter_kernel(const int32_t* __restrict__ bucket, int n, int B, int ntiles, int
   __shared__ int s_wc[kWarps][kMaxBuckets];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int b = tid; b < B; b += kThreads) {
-    s_run[b] = offs[b * ntiles + blockIdx.x];
+    s_run[b] = offs[b * ntiles + blockIdx.x * col_stride];
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) s_wc[w][b] = 0;
   }
@@ -299,7 +310,7 @@ scatter_kernel(const int32_t* __restrict__ bucket, int n, int B, int ntiles, int
   const int base = blockIdx.x * tile;
   for (int c = 0; c < tile && base + c < n; c += kThreads) {
     const int i = base + c + tid;
-    const bool valid = i < n;
+    const bool valid = i < n && c + tid < tile;
     const int b = valid ? bucket[i] : -1;
     const unsigned peers = __match_any_sync(0xffffffffu, b);
     const int rank = __popc(peers & lanemask_lt());
@@ -508,26 +519,27 @@ cudaError_t launch_predict_shuffle(const smoe_desc& d, const int32_t* ids, const
   DeviceStatus* st = ws_ptr<DeviceStatus>(ws, L.status);
   int32_t* hist = ws_ptr<int32_t>(ws, L.sort_hist);
   int32_t* offs = ws_ptr<int32_t>(ws, L.sort_off);
-  const int ntiles = ceil_div(d.T, kShufTile);
-  cudaError_t e = cudaMemsetAsync(hist, 0, sizeof(int32_t) * d.P * ntiles, s);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(predict_hist_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)predict_smem(d.E));
+  // histogram columns of kPredTokens tokens (one per predict CTA, written directly);
+  // scatter tiles of kShufScatter tokens
+  const int ntiles = ceil_div(d.T, kPredTokens);
+  constexpr int kStride = kShufScatter / kPredTokens;
+  cudaError_t e = cudaFuncSetAttribute(predict_hist_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)predict_smem(d.E));
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(predict_hist_kernel<true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)predict_smem(d.E));
   if (e != cudaSuccess) return e;
   if (prev_cluster)
-    SMOE_LAUNCH(predict_hist_kernel<true>, ceil_div(d.T, kPredTokens), kThreads, predict_smem(d.E),
-        s, ids, conf, emap, d.T, d.E, d.P, d.vocab, pred, hist, ntiles, st, prev_cluster,
-        table_a, d.K);
+    SMOE_LAUNCH(predict_hist_kernel<true>, ntiles, kThreads, predict_smem(d.E), s, ids, conf,
+        emap, d.T, d.E, d.P, d.vocab, pred, hist, ntiles, kPredTokens, st, prev_cluster, table_a,
+        d.K);
   else
-    SMOE_LAUNCH(predict_hist_kernel<false>, ceil_div(d.T, kPredTokens), kThreads,
-        predict_smem(d.E), s, ids, conf, emap, d.T, d.E, d.P, d.vocab, pred, hist, ntiles, st,
-        nullptr, nullptr, d.K);
+    SMOE_LAUNCH(predict_hist_kernel<false>, ntiles, kThreads, predict_smem(d.E), s, ids, conf,
+        emap, d.T, d.E, d.P, d.vocab, pred, hist, ntiles, kPredTokens, st, nullptr, nullptr, d.K);
   SMOE_LAUNCH(scan_kernel, 1, 1024, 0, s, hist, offs, d.P * ntiles, d.P, ntiles, d.T, part_off);
-  SMOE_LAUNCH(scatter_kernel<kShuffle>, ntiles, kThreads, 0, s, pred, d.T, d.P, ntiles, kShufTile,
-      offs, perm, nullptr, 0, 0, nullptr, nullptr, nullptr);
+  SMOE_LAUNCH(scatter_kernel<kShuffle>, ceil_div(d.T, kShufScatter), kThreads, 0, s, pred, d.T,
+      d.P, ntiles, kShufScatter, kStride, offs, perm, nullptr, 0, 0, nullptr, nullptr, nullptr);
   if (x_shuf) {
     const int vec = (int)(d.d * elem_size(d) / 16);
     SMOE_LAUNCH(gather_rows_kernel, grid_for_rows(d.T), kThreads, 0, s,
@@ -555,7 +567,7 @@ cudaError_t launch_dispatch(const smoe_desc& d, const int32_t* idx, const int32_
   SMOE_LAUNCH(dispatch_hist_kernel, ntiles, kThreads, 0, s, idx, perm, d.T, d.K, d.E, bucket, hist,
       ntiles, tile, st);
   SMOE_LAUNCH(scan_kernel, 1, 1024, 0, s, hist, offs, d.E * ntiles, d.E, ntiles, n, expert_off);
-  SMOE_LAUNCH(scatter_kernel<kDispatch>, ntiles, kThreads, 0, s, bucket, n, d.E, ntiles, tile,
+  SMOE_LAUNCH(scatter_kernel<kDispatch>, ntiles, kThreads, 0, s, bucket, n, d.E, ntiles, tile, 1,
       offs, nullptr, perm, d.T, d.K, pair_row, row_token, row_src);
   if (x_disp) {
     const int vec = (int)(d.d * elem_size(d) / 16);
@@ -675,11 +687,11 @@ extern "C" SMOE_API int smoe_predict_shuffle_noalloc(const smoe_desc* desc,
   if (ce != cudaSuccess) return set_last_error(SMOE_ERR_CUDA, cudaGetErrorString(ce));
   SMOE_LAUNCH_STATUS(predict_hist_kernel<false>, ceil_div(d.T, kPredTokens), kThreads,
       predict_smem(d.E), s, token_ids, conf, expert_part, d.T, d.E, d.P, d.vocab, pred_part, hist,
-      ntiles, nullptr, nullptr, nullptr, d.K);
+      ntiles, kShufTile, nullptr, nullptr, nullptr, d.K);
   SMOE_LAUNCH_STATUS(scan_kernel, 1, 1024, 0, s, hist, offs, d.P * ntiles, d.P, ntiles, d.T,
       part_off);
   SMOE_LAUNCH_STATUS(scatter_kernel<kShuffle>, ntiles, kThreads, 0, s, pred_part, d.T, d.P, ntiles,
-      kShufTile, offs, shuf_perm, nullptr, 0, 0, nullptr, nullptr, nullptr);
+      kShufTile, 1, offs, shuf_perm, nullptr, 0, 0, nullptr, nullptr, nullptr);
   if (x_shuf) {
     const int vec = (int)(d.d * elem_size(d) / 16);
     SMOE_LAUNCH_STATUS(gather_rows_kernel, grid_for_rows(d.T), kThreads, 0, s,
