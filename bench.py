@@ -113,14 +113,16 @@ def source_hash(*names) -> str:
     return h.hexdigest()[:16]
 
 
-def stage_bytes(cfg) -> dict:
-    """Algorithmic bytes per stage (each input read once, each output written once)."""
+def stage_bytes(cfg, rows_in_ffn: bool = False) -> dict:
+    """Algorithmic bytes per stage (each input read once, each output written once). With
+    rows_in_ffn the dispatch stage only sorts (indices in, pair_row / row_token / row_slot
+    out) and its row copy runs inside the expert FFN's up GEMM."""
     T, d, E, K, S, b = cfg.T, cfg.d, cfg.E, cfg.K, cfg.n_shared, cfg.elem_bytes
     return {
         "route": T * d * b + E * d * b + T * E * 4 + T * K * 8,
         "predict_shuffle": T * 4 + T * E * 4 + 2 * T * d * b + 3 * T * 4,
         "lar": T * K * 4 + T * 4,
-        "dispatch": 2 * T * K * d * b + T * K * 12,
+        "dispatch": (T * K * 16 if rows_in_ffn else 2 * T * K * d * b + T * K * 12),
         "combine": T * K * d * b + S * T * d * b + T * K * 8 + T * d * b,
     }
 
@@ -272,6 +274,9 @@ class Workload:
         self.row_token = torch.empty(T * K, **i32)
         self.x_shuf = torch.empty_like(self.x)
         self.x_disp = torch.empty(T * K, cfg.d, dtype=self.x.dtype, device=dev)
+        self.row_slot = torch.empty(T * K, **i32)
+        # the library copies the dispatched rows inside the up GEMM for this layer shape
+        self.rows_in_ffn = smoe.smoe_expert_ffn_gather_fused(self.desc)
         self.y_sh = (torch.empty(cfg.n_shared, T, cfg.d, dtype=self.x.dtype, device=dev)
                      if cfg.n_shared else None)
         self.y = torch.empty_like(self.x)
@@ -342,11 +347,19 @@ class Workload:
         rec(1)
         s.smoe_lar(c.desc, c.idx, c.emap_d, c.lar, c.ws, src_part=c.pred)
         rec(2)
-        s.smoe_dispatch(c.desc, c.idx, c.expert_off, c.pair_row, c.row_token, c.ws,
-                        shuf_perm=c.perm, x_src=c.x_shuf, x_disp=c.x_disp)
-        rec(3)
-        s.smoe_expert_ffn(c.desc, c.x_disp, c.expert_off, c.w1, c.w3, c.w2, c.x_disp, c.ws,
-                          x=c.x, y_shared=c.y_sh)
+        if c.rows_in_ffn:
+            # the dispatch sorts; the FFN copies the rows inside its up GEMM
+            s.smoe_dispatch(c.desc, c.idx, c.expert_off, c.pair_row, c.row_token, c.ws,
+                            shuf_perm=c.perm, row_slot=c.row_slot)
+            rec(3)
+            s.smoe_expert_ffn_gather(c.desc, c.x_shuf, c.row_slot, c.x_disp, c.expert_off, c.w1,
+                                     c.w3, c.w2, c.x_disp, c.ws, x=c.x, y_shared=c.y_sh)
+        else:
+            s.smoe_dispatch(c.desc, c.idx, c.expert_off, c.pair_row, c.row_token, c.ws,
+                            shuf_perm=c.perm, x_src=c.x_shuf, x_disp=c.x_disp)
+            rec(3)
+            s.smoe_expert_ffn(c.desc, c.x_disp, c.expert_off, c.w1, c.w3, c.w2, c.x_disp, c.ws,
+                              x=c.x, y_shared=c.y_sh)
         rec(4)
         s.smoe_combine(c.desc, c.x_disp, c.pair_row, c.w, c.y, c.ws, y_shared=c.y_sh)
         rec(5)
@@ -589,6 +602,9 @@ def run_native(args):
         if tj.get("source_hash") == source_hash("ffn.cu"):
             traffic = tj.get("workloads", {}).get(cfg.name, {}).get("bytes_per_step")
     kernel_name = "expert_ffn (grouped SwiGLU up + down GEMMs)"
+    if wl.rows_in_ffn:
+        kernel_name = ("expert_ffn (grouped SwiGLU up + down GEMMs, the dispatch's row copy "
+                       "inside the up GEMM)")
     if ffn_flops(cfg) / fbytes >= peak_tf * 1e12 / (hbm * 1e9):
         roofline = {"bound": "tensor", "achieved": round(achieved_tf, 2), "peak": peak_tf,
                     "unit": "TFLOP/s", "frac": round(achieved_tf / peak_tf, 4),
@@ -600,7 +616,7 @@ def run_native(args):
                     "unit": "GB/s", "frac": round(achieved_gbs / hbm, 4), "traffic": traffic,
                     "kernel": kernel_name, "peak_kind": f"{peaks_kind} HBM copy",
                     "algorithmic_bytes": fbytes, "experts_touched": touched}
-    sb = stage_bytes(cfg)
+    sb = stage_bytes(cfg, wl.rows_in_ffn)
     stages = {}
     for k, ms in stage_ms.items():
         ent = {"ms": round(ms, 4)}
@@ -609,6 +625,8 @@ def run_native(args):
             ent.update({"GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4)})
         stages[k] = ent
     stages["expert_ffn"]["TFLOP/s"] = round(achieved_tf, 2)
+    if wl.rows_in_ffn:
+        stages["dispatch"]["rows"] = "sort only; the row copy runs inside the expert_ffn up GEMM"
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

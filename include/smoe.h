@@ -219,6 +219,30 @@ SMOE_API int smoe_expert_ffn(const smoe_desc* desc, const void* x_disp, const vo
                              const void* w2, void* y_disp, void* y_shared, void* ws,
                              size_t ws_bytes, void* stream);
 
+/* a6 + a7/a8 -- the dispatch's row copy and the expert FFN in one call: X_disp[r] =
+ * x_src[row_slot[r]] for the T K dispatched rows, then the FFN of smoe_expert_ffn on
+ * them. Where smoe_expert_ffn_gather_fused says so (bf16 two-SM tiles, at least 256 rows
+ * per expert on average, F <= 1024) the copy runs inside the up GEMM, chunk by chunk
+ * ahead of the tiles that read it, so the write-bound copy overlaps the tensor-core
+ * work; otherwise it runs as a separate copy first.
+ * Same results as smoe_dispatch(x_disp) followed by smoe_expert_ffn.
+ *   x_src      [T, d] dtype rows (x_shuf, or x without a shuffle)
+ *   row_slot   [T K] int32 in [0, T) (smoe_dispatch's row_slot output)
+ *   x_disp     [T K, d] dtype, written (the gathered rows); may be the same buffer as
+ *              y_disp, which the down GEMM writes after the up GEMM has read it
+ *   x, expert_off, w1, w3, w2, y_disp, y_shared as in smoe_expert_ffn.
+ * An out-of-range row_slot entry gives a zero row and SMOE_ERR_DATA in the status; a
+ * copy that is not published within the device wait limit gives SMOE_ERR_DEVICE_TIMEOUT. */
+SMOE_API int smoe_expert_ffn_gather(const smoe_desc* desc, const void* x_src,
+                                    const int32_t* row_slot, const void* x, void* x_disp,
+                                    const int32_t* expert_off, const void* w1, const void* w3,
+                                    const void* w2, void* y_disp, void* y_shared, void* ws,
+                                    size_t ws_bytes, void* stream);
+
+/* 1 when smoe_expert_ffn_gather copies the rows inside the up GEMM for this layer shape,
+ * 0 when it copies them before the FFN (or the descriptor is invalid). Host only. */
+SMOE_API int smoe_expert_ffn_gather_fused(const smoe_desc* desc);
+
 /* a9 -- combine ("Speculative MoE" §1: results return to the token's source;
  * FoE: per-group results are summed): y[t] = sum_{k=0}^{K-1} w[t,k] y_disp[pair_row[t,k]]
  * + sum_j y_shared[j, t], accumulated in fp32 in exactly that order, one writer per

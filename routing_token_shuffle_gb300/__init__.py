@@ -6,7 +6,8 @@ ABI of ``include/smoe.h``); ``binding`` forwards tensors to it. Build it with
 """
 from .binding import (  # noqa: F401
     SMOE_BF16, SMOE_F32, LayerIO, LayerWeights, SmoeDesc, SmoeError, desc_from_config, kernel_launches, layer_io,
-    layer_weights, lib, make_desc, smoe_combine, smoe_dispatch, smoe_expert_ffn, smoe_get_status,
+    layer_weights, lib, make_desc, smoe_combine, smoe_dispatch, smoe_expert_ffn, smoe_expert_ffn_gather,
+    smoe_expert_ffn_gather_fused, smoe_get_status,
     smoe_lar, smoe_layer_forward, smoe_moe_forward_routed, smoe_layer_forward_host, smoe_predict_shuffle,
     smoe_predict_shuffle_inter, smoe_prefetch_predict, smoe_route, smoe_selftest_device_timeout,
     smoe_token_cluster, workspace, workspace_size)

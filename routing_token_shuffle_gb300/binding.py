@@ -59,6 +59,9 @@ SIGNATURES = {
                                                   _SZ, _P]),
     "smoe_dispatch": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "smoe_expert_ffn": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "smoe_expert_ffn_gather": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                              _SZ, _P]),
+    "smoe_expert_ffn_gather_fused": (ctypes.c_int, [_D]),
     "smoe_combine": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "smoe_layer_forward": (ctypes.c_int, [_D, ctypes.POINTER(LayerWeights),
                                           ctypes.POINTER(LayerIO), _P, _SZ, _P]),
@@ -197,6 +200,18 @@ def smoe_expert_ffn(desc, x_disp, expert_off, w1, w3, w2, y_disp, ws, x=None, y_
     _check(lib().smoe_expert_ffn(ctypes.byref(desc), _ptr(x_disp), _ptr(x), _ptr(expert_off),
                                  _ptr(w1), _ptr(w3), _ptr(w2), _ptr(y_disp), _ptr(y_shared),
                                  _ptr(ws), ws.numel(), _stream(stream)), "smoe_expert_ffn")
+
+
+def smoe_expert_ffn_gather(desc, x_src, row_slot, x_disp, expert_off, w1, w3, w2, y_disp, ws,
+                           x=None, y_shared=None, stream=None):
+    _check(lib().smoe_expert_ffn_gather(ctypes.byref(desc), _ptr(x_src), _ptr(row_slot), _ptr(x),
+                                        _ptr(x_disp), _ptr(expert_off), _ptr(w1), _ptr(w3),
+                                        _ptr(w2), _ptr(y_disp), _ptr(y_shared), _ptr(ws),
+                                        ws.numel(), _stream(stream)), "smoe_expert_ffn_gather")
+
+
+def smoe_expert_ffn_gather_fused(desc) -> bool:
+    return bool(lib().smoe_expert_ffn_gather_fused(ctypes.byref(desc)))
 
 
 def smoe_combine(desc, y_disp, pair_row, topk_w, y_out, ws, y_shared=None, stream=None):

@@ -152,6 +152,7 @@ bool ws_layout(const smoe_desc& d, WsLayout* L) {
   // the prefetch predictor routes 2T rows in one launch
   L->route_part = take(4 * E * std::max((size_t)route_splits(d, d.T) * T,
                                         (size_t)route_splits(d, 2 * d.T) * 2 * T));
+  L->gather_flags = take(4 * ((T * K + 63) / 64 + 2));   // 64-row block counts + ticket
   L->total = off;
   return true;
 }
@@ -355,6 +356,39 @@ SMOE_API int smoe_expert_ffn(const smoe_desc* desc, const void* x_disp, const vo
   return SMOE_OK;
 }
 
+SMOE_API int smoe_expert_ffn_gather(const smoe_desc* desc, const void* x_src,
+                                    const int32_t* row_slot, const void* x, void* x_disp,
+                                    const int32_t* expert_off, const void* w1, const void* w3,
+                                    const void* w2, void* y_disp, void* y_shared, void* ws,
+                                    size_t ws_bytes, void* stream) {
+  SMOE_CHECK(check_desc(desc));
+  SMOE_PTR(x_src);
+  SMOE_PTR(row_slot);
+  SMOE_PTR(x_disp);
+  SMOE_PTR(expert_off);
+  SMOE_PTR(w1);
+  SMOE_PTR(w3);
+  SMOE_PTR(w2);
+  SMOE_PTR(y_disp);
+  if (desc->n_shared > 0) {
+    SMOE_PTR(x);
+    SMOE_PTR(y_shared);
+  }
+  SMOE_CHECK(check_ws(desc, ws, ws_bytes));
+  SMOE_CHECK(check_device());
+  if (desc->T == 0) return SMOE_OK;
+  const FfnGather g{x_src, row_slot, desc->T};
+  cudaError_t e = launch_expert_ffn(*desc, x_disp, x, expert_off, w1, w3, w2, y_disp, y_shared,
+                                    ws, static_cast<cudaStream_t>(stream), &g);
+  if (e != cudaSuccess) return cuda_fail(e, "expert ffn launch");
+  return SMOE_OK;
+}
+
+SMOE_API int smoe_expert_ffn_gather_fused(const smoe_desc* desc) {
+  if (check_desc(desc) != SMOE_OK) return 0;
+  return ffn_gather_in_gemm(*desc) ? 1 : 0;
+}
+
 SMOE_API int smoe_combine(const smoe_desc* desc, const void* y_disp, const int32_t* pair_row,
                           const float* topk_w, const void* y_shared, void* y_out, void* ws,
                           size_t ws_bytes, void* stream) {
@@ -401,10 +435,15 @@ static int layer_forward_impl(const smoe_desc* d, const smoe_layer_weights* W,
     if (e != cudaSuccess) return cuda_fail(e, "lar launch");
   }
   const void* x_src = io->skip_shuffle ? io->x : x_shuf;
+  // the dispatch sorts the pairs; the FFN copies the rows (inside its up GEMM when it
+  // runs two-SM tiles)
+  int32_t* row_slot = ws_ptr<int32_t>(ws, L.row_src);
   e = launch_dispatch(*d, idx, io->skip_shuffle ? nullptr : perm, x_src, expert_off, pair_row,
-                      row_token, nullptr, x_disp, ws, s);
+                      row_token, row_slot, nullptr, ws, s);
   if (e != cudaSuccess) return cuda_fail(e, "dispatch launch");
-  e = launch_expert_ffn(*d, x_disp, io->x, expert_off, W->w1, W->w3, W->w2, y_disp, y_sh, ws, s);
+  const FfnGather g{x_src, row_slot, d->T};
+  e = launch_expert_ffn(*d, x_disp, io->x, expert_off, W->w1, W->w3, W->w2, y_disp, y_sh, ws, s,
+                        &g);
   if (e != cudaSuccess) return cuda_fail(e, "expert ffn launch");
   e = launch_combine(*d, y_disp, pair_row, w, y_sh, io->y, ws, s);
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
@@ -498,10 +537,12 @@ SMOE_API int smoe_moe_forward_routed(const smoe_desc* desc, const void* x,
   int32_t* row_token = ws_ptr<int32_t>(ws, L.row_token);
   void* x_disp = ws_ptr<char>(ws, L.x_disp);
   void* y_sh = desc->n_shared ? ws_ptr<char>(ws, L.y_sh) : nullptr;
+  int32_t* row_slot = ws_ptr<int32_t>(ws, L.row_src);
   cudaError_t e = launch_dispatch(*desc, topk_idx, nullptr, x, expert_off, pair_row, row_token,
-                                  nullptr, x_disp, ws, s);
+                                  row_slot, nullptr, ws, s);
   if (e != cudaSuccess) return cuda_fail(e, "dispatch launch");
-  e = launch_expert_ffn(*desc, x_disp, x, expert_off, w1, w3, w2, x_disp, y_sh, ws, s);
+  const FfnGather g{x, row_slot, desc->T};
+  e = launch_expert_ffn(*desc, x_disp, x, expert_off, w1, w3, w2, x_disp, y_sh, ws, s, &g);
   if (e != cudaSuccess) return cuda_fail(e, "expert ffn launch");
   e = launch_combine(*desc, x_disp, pair_row, topk_w, y_sh, y, ws, s);
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");

@@ -87,9 +87,11 @@ __device__ __forceinline__ int clamp_rows(int v) { return v < 0 ? 0 : (v > 32 ? 
 // word records the error.
 __global__ void tile_table_kernel(const int32_t* __restrict__ expert_off, int E, int n_shared,
                                   int T, int TK, int bm, int32_t* __restrict__ tile_start,
-                                  DeviceStatus* st) {
+                                  DeviceStatus* st, int32_t* __restrict__ g_flags, int g_n) {
   pdl_wait_and_trigger();
   const int lane = threadIdx.x;
+  // gather mode: clear the ready flags and the chunk ticket of the up GEMM that follows
+  for (int i = lane; i < g_n; i += 32) g_flags[i] = 0;
   const int G = E + n_shared;
   bool bad = false;
   for (int g = lane; g < E; g += 32) {
@@ -121,6 +123,9 @@ __global__ void tile_table_kernel(const int32_t* __restrict__ expert_off, int E,
   if (lane == 0) tile_start[G] = carry;
 }
 
+// In-GEMM row gather (see gather_worker): rows per completion counter.
+constexpr int kGatherBlock = 64;
+
 struct GemmArgs {
   const int32_t* expert_off;  // [E+1]
   const int32_t* tile_start;  // [G+1] m-tiles per group, prefix
@@ -131,6 +136,16 @@ struct GemmArgs {
   int N;                      // output columns: F (up) or d (down)
   int KD;                     // contraction length: d (up) or F (down)
   int NT;                     // n-tiles
+  // gather mode (two-SM up GEMM): X_disp[r] = g_src[g_map[r]] is written by this kernel's
+  // gather warps while it runs, in chunks of g_chunk rows (a power of two <= 32);
+  // g_counts[b] counts the written rows of 64-row block b; *g_ticket numbers the chunks
+  // taken. g_src == nullptr: X_disp is already in place.
+  const uint4* g_src;
+  const int32_t* g_map;
+  uint4* g_dst;
+  int32_t* g_ticket;
+  int32_t* g_counts;
+  int g_vec, g_nsrc, g_nchunks, g_chunk;
 };
 
 struct Tile {
@@ -367,6 +382,73 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   if (warp == 2) tc::tmem_dealloc(tmem, 2 * kAccCols);
 }
 
+// ------------------------------------------------------------------ in-GEMM gather
+// Gather mode hides the dispatch's row copy (X_disp[r] = x_src[row_slot[r]], a write-bound
+// stream) under the up GEMM, which leaves DRAM mostly idle. Gather warps of every CTA take
+// chunks of g_chunk rows (about 16 KB) from a global ticket, in row order (the order in
+// which the tiles consume them), copy them and add their row count to the counter of
+// their 64-row block; a TMA producer waits (bounded) until the blocks of its tile's own
+// rows are complete, then orders the async proxy after the generic writes before
+// loading. A claimed chunk is always being copied by a running CTA, and unclaimed chunks
+// are claimed by any running CTA, the waiting one included, so no CTA waits on one that
+// has not started.
+__device__ __forceinline__ void gather_worker(const GemmArgs& p, int lane) {
+  for (;;) {
+    int c = 0;
+    if (lane == 0) c = atomicAdd(p.g_ticket, 1);
+    c = __shfl_sync(0xffffffffu, c, 0);
+    if (c >= p.g_nchunks) break;
+    const int r0 = c * p.g_chunk;
+    const int nr = min(p.g_chunk, p.TK - r0);
+    const int my_src = lane < nr ? p.g_map[r0 + lane] : 0;
+    for (int i = 0; i < nr; ++i) {
+      const int srow = __shfl_sync(0xffffffffu, my_src, i);
+      uint4* out = p.g_dst + (size_t)(r0 + i) * p.g_vec;
+      if ((unsigned)srow >= (unsigned)p.g_nsrc) {
+        if (lane == 0) record_error(p.st, kStatusData, kBadPerm, r0 + i);
+        for (int v = lane; v < p.g_vec; v += 32) out[v] = make_uint4(0, 0, 0, 0);
+        continue;
+      }
+      const uint4* in = p.g_src + (size_t)srow * p.g_vec;
+      for (int v = lane; v < p.g_vec; v += 32 * 8) {
+        uint4 t[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (v + 32 * u < p.g_vec) t[u] = __ldg(in + v + 32 * u);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (v + 32 * u < p.g_vec) out[v + 32 * u] = t[u];
+      }
+    }
+    __threadfence();  // each lane's row writes, before the warp's count
+    __syncwarp();
+    if (lane == 0) atomicAdd(p.g_counts + r0 / kGatherBlock, nr);
+  }
+}
+
+// Wait until rows [lo, hi) of X_disp are written (their 64-row blocks complete); false
+// after the bounded wait (or when another role of the CTA gave up).
+__device__ __forceinline__ bool wait_rows(const GemmArgs& p, int lo, int hi, volatile int* abort) {
+  if (hi <= lo) return true;
+  for (int b = lo / kGatherBlock; b <= (hi - 1) / kGatherBlock; ++b) {
+    const int32_t* f = p.g_counts + b;
+    const int want = min(kGatherBlock, p.TK - b * kGatherBlock);
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    if (v >= want) continue;
+    const unsigned long long t0 = tc::globaltimer();
+    for (uint32_t i = 1;; ++i) {
+      __nanosleep(64);
+      asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+      if (v >= want) break;
+      if ((i & 63u) == 0 && (*abort || tc::globaltimer() - t0 > tc::kWaitTimeoutNs)) return false;
+    }
+  }
+  // the rows were written through the generic proxy; TMA reads through the async proxy
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return true;
+}
+
 // ------------------------------------------------------------------ two-SM variant
 // A cluster of two CTAs (on the two SMs of a TPC) computes 256 x 256 tiles with
 // tcgen05.mma.cta_group::2: each CTA loads its own 128 rows of A and 128 rows of B, so
@@ -381,6 +463,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 // `full` barrier; MMA completion is multicast to both CTAs' `empty` and `tfull`; both
 // epilogues drain their own TMEM lanes and arrive on the leader's `tempty`.
 constexpr int kPairStages = 6;
+// warps 0-7 as in the single-SM kernel; warps 2, 3 and 8-11 copy rows in gather mode
+constexpr int kPairThreads = 384;
 constexpr uint32_t kPairStage = 128 * 128;  // A half or B half: 128 rows x 128 bytes
 constexpr size_t kPairSmemBytes = 1024 + kPairStages * 2 * kPairStage + kStageOut + 256 +
                                   4 * (kMaxGroups + 1 + 513 + 4);
@@ -422,7 +506,7 @@ __device__ __forceinline__ void decode_pair_tile(const int32_t* ts, const int32_
 }
 
 template <bool UP>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kPairThreads, 1)
 grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,     // 128-row box
                          const __grid_constant__ CUtensorMap tmA_sh,  // 128-row box
                          const __grid_constant__ CUtensorMap tmA64,   // 64-row box
@@ -472,8 +556,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,     // 128-row
     tc::tma_prefetch_map(&tmB1);
     tc::tma_prefetch_map(&tmB3);
   }
-  for (int i = threadIdx.x; i <= p.G; i += kThreads) s_ts[i] = p.tile_start[i];
-  for (int i = threadIdx.x; i <= p.E; i += kThreads) s_eo[i] = p.expert_off[i];
+  for (int i = threadIdx.x; i <= p.G; i += kPairThreads) s_ts[i] = p.tile_start[i];
+  for (int i = threadIdx.x; i <= p.E; i += kPairThreads) s_eo[i] = p.expert_off[i];
   if (warp == 2) {
     tc::tmem_alloc_pair(s_tmem, 2 * kAccCols);
     tc::tmem_relinquish_pair();
@@ -497,6 +581,11 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,     // 128-row
       const CUtensorMap* amap = tl.m128 ? (tl.a_shared ? &tmA_sh64 : &tmA64)
                                         : (tl.a_shared ? &tmA_sh : &tmA);
       const uint32_t tx = 2 * ((tl.m128 ? kPairStage / 2 : kPairStage) + kPairStage);
+      if (UP && p.g_src && !tl.a_shared &&
+          !wait_rows(p, tl.a_row, min(tl.a_row + (tl.m128 ? 64 : 128), s_eo[tl.g + 1]), abort)) {
+        ok = false;
+        break;
+      }
       for (int kb = 0; kb < nkb; ++kb, ++it) {
         const uint32_t s = it % kPairStages, ph = (it / kPairStages) & 1u;
         if (!tc::mbar_wait(&empty[s], ph ^ 1u, abort)) { ok = false; break; }
@@ -546,7 +635,10 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,     // 128-row
     volatile int never = 0;
     tc::commit_pair(drain, 0x1);
     tc::mbar_wait(drain, 0, &never);
-  } else if (warp >= 4) {
+  } else if (UP && p.g_src && (warp == 2 || warp == 3 || warp >= 8)) {
+    // ---------------------------------------------------------------- row gather
+    gather_worker(p, lane);
+  } else if (warp >= 4 && warp < 8) {
     // ---------------------------------------------------------------- epilogue (both CTAs)
     const int q = warp & 3;
     uint32_t tcount = 0;
@@ -659,7 +751,7 @@ cudaError_t launch_gemm_pair(const CUtensorMap& A, const CUtensorMap& Ash, const
   const int pairs = (int)std::min<long long>(sm_count() / 2, std::max<long long>(tile_bound, 1));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kPairThreads);
   cfg.dynamicSmemBytes = kPairSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -684,10 +776,21 @@ bool use_pair_tiles(const smoe_desc& d) {
   return d.dtype == SMOE_BF16 && (long long)d.T * d.K >= (long long)kPairMinRows * d.E;
 }
 
+}  // namespace
+
+// The row copy runs inside the up GEMM on two-SM tiles with F <= 1024: the copied bytes
+// per FFN flop are b / (6 F), so small experts gain most. Measured (dispatch + FFN, same
+// session): F = 768 (Qwen3 shape) -6 %, F = 1536 (DeepSeek-V2) within 1 %, F = 14336
+// (Mixtral) +2.5 %: there the power-capped GEMM loses more to the concurrent copy than
+// the copy's own time.
+bool ffn_gather_in_gemm(const smoe_desc& d) { return use_pair_tiles(d) && d.F <= 1024; }
+
+namespace {
+
 template <bool F32>
 cudaError_t run_ffn(const smoe_desc& d, const void* x_disp, const void* x,
                     const int32_t* expert_off, const void* w1, const void* w3, const void* w2,
-                    void* y_disp, void* y_sh, void* ws, cudaStream_t s) {
+                    void* y_disp, void* y_sh, void* ws, cudaStream_t s, const FfnGather* gather) {
   WsLayout L;
   ws_layout(d, &L);
   int32_t* tiles = ws_ptr<int32_t>(ws, L.tiles);
@@ -697,7 +800,21 @@ cudaError_t run_ffn(const smoe_desc& d, const void* x_disp, const void* x,
   const uint32_t box_k = F32 ? 32 : 64;
   const bool pairs = !F32 && use_pair_tiles(d);
   const int bm = pairs ? 256 : kBM;
-  SMOE_LAUNCH(tile_table_kernel, 1, 32, 0, s, expert_off, d.E, d.n_shared, d.T, TK, bm, tiles, st);
+  if (gather && !ffn_gather_in_gemm(d)) {  // copy the rows first
+    cudaError_t e = launch_gather_rows(d, gather->src, gather->map, TK, gather->nsrc,
+                                       const_cast<void*>(x_disp), ws, s);
+    if (e != cudaSuccess) return e;
+    gather = nullptr;
+  }
+  // gather chunks of about 16 KB of rows: many warps copy the rows of the first tiles
+  // in parallel
+  const int row_bytes = (int)(d.d * elem_size(d));
+  int chunk = 1;
+  while (chunk < 32 && (chunk * 2) * row_bytes <= 16384) chunk *= 2;  // <= 32: a lane per row
+  const int nchunks = ceil_div(TK, chunk), nblocks = ceil_div(TK, kGatherBlock);
+  int32_t* gflags = ws_ptr<int32_t>(ws, L.gather_flags);  // [nblocks] counts, then the ticket
+  SMOE_LAUNCH(tile_table_kernel, 1, 32, 0, s, expert_off, d.E, d.n_shared, d.T, TK, bm, tiles, st,
+              gflags, gather ? nblocks + 1 : 0);
 
   const long long mtile_bound =
       ceil_div(TK, bm) + d.E + (long long)d.n_shared * ceil_div(d.T, bm);
@@ -705,6 +822,17 @@ cudaError_t run_ffn(const smoe_desc& d, const void* x_disp, const void* x,
   const void* x_src = d.n_shared ? x : x_disp;
   const uint64_t h_rows = (uint64_t)TK + (uint64_t)d.n_shared * d.T;
   GemmArgs up{expert_off, tiles, hbuf, nullptr, st, d.E, G, d.T, TK, d.F, d.d, ceil_div(d.F, 128)};
+  if (gather) {
+    up.g_src = static_cast<const uint4*>(gather->src);
+    up.g_map = gather->map;
+    up.g_dst = static_cast<uint4*>(const_cast<void*>(x_disp));
+    up.g_counts = gflags;
+    up.g_ticket = gflags + nblocks;
+    up.g_vec = row_bytes / 16;
+    up.g_nsrc = gather->nsrc;
+    up.g_nchunks = nchunks;
+    up.g_chunk = chunk;
+  }
   GemmArgs dn{expert_off, tiles, y_disp, y_sh, st, d.E, G, d.T, TK, d.d, d.F, ceil_div(d.d, 256)};
 
   if (pairs) {
@@ -796,10 +924,10 @@ bool encode_tmap_2d(CUtensorMap* map, const void* base, bool fp32, uint64_t rows
 cudaError_t launch_expert_ffn(const smoe_desc& d, const void* x_disp, const void* x,
                               const int32_t* expert_off, const void* w1, const void* w3,
                               const void* w2, void* y_disp, void* y_sh, void* ws,
-                              cudaStream_t s) {
+                              cudaStream_t s, const FfnGather* gather) {
   if (d.dtype == SMOE_F32)
-    return run_ffn<true>(d, x_disp, x, expert_off, w1, w3, w2, y_disp, y_sh, ws, s);
-  return run_ffn<false>(d, x_disp, x, expert_off, w1, w3, w2, y_disp, y_sh, ws, s);
+    return run_ffn<true>(d, x_disp, x, expert_off, w1, w3, w2, y_disp, y_sh, ws, s, gather);
+  return run_ffn<false>(d, x_disp, x, expert_off, w1, w3, w2, y_disp, y_sh, ws, s, gather);
 }
 
 }  // namespace smoe

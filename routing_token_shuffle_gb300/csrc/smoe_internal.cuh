@@ -89,6 +89,7 @@ struct WsLayout {
   size_t x_dev, ids_dev, y_dev;     // staging for smoe_layer_forward_host
   size_t pf_qs, pf_logits, pf_idx;  // prefetch predictor: q and s rows, logits, routes
   size_t route_part;                // gate GEMM partial logits [KS, T, E]
+  size_t gather_flags;              // in-GEMM row gather: chunk ready flags + ticket
   size_t total;
 };
 
@@ -200,10 +201,23 @@ cudaError_t launch_dispatch(const smoe_desc& d, const int32_t* idx, const int32_
                             int32_t* row_token, int32_t* row_slot, void* x_disp, void* ws,
                             cudaStream_t s);
 
+// gather != nullptr: x_disp is an output, X_disp[r] = gather->src[gather->map[r]] for the
+// T K dispatched rows, copied inside the up GEMM when ffn_gather_in_gemm (otherwise by a
+// row-gather launch before it).
+struct FfnGather {
+  const void* src;     // [nsrc, d] rows (x_shuf or x)
+  const int32_t* map;  // [T K] source row of each dispatched row
+  int nsrc;
+};
 cudaError_t launch_expert_ffn(const smoe_desc& d, const void* x_disp, const void* x,
                               const int32_t* expert_off, const void* w1, const void* w3,
                               const void* w2, void* y_disp, void* y_sh, void* ws,
-                              cudaStream_t s);
+                              cudaStream_t s, const FfnGather* gather = nullptr);
+// true when launch_expert_ffn with a gather copies the rows inside its up GEMM
+bool ffn_gather_in_gemm(const smoe_desc& d);
+// dst[r] = src[map[r]] for nrows rows of d elements (16-byte vectors)
+cudaError_t launch_gather_rows(const smoe_desc& d, const void* src, const int32_t* map,
+                               int nrows, int nsrc, void* dst, void* ws, cudaStream_t s);
 
 cudaError_t launch_combine(const smoe_desc& d, const void* y_disp, const int32_t* pair_row,
                            const float* w, const void* y_sh, void* y, void* ws, cudaStream_t s);

@@ -577,6 +577,17 @@ cudaError_t launch_dispatch(const smoe_desc& d, const int32_t* idx, const int32_
   return cudaGetLastError();
 }
 
+cudaError_t launch_gather_rows(const smoe_desc& d, const void* src, const int32_t* map,
+                               int nrows, int nsrc, void* dst, void* ws, cudaStream_t s) {
+  WsLayout L;
+  ws_layout(d, &L);
+  const int vec = (int)(d.d * elem_size(d) / 16);
+  SMOE_LAUNCH(gather_rows_kernel, grid_for_rows(nrows), kThreads, 0, s,
+      static_cast<const uint4*>(src), static_cast<uint4*>(dst), map, nrows, nsrc, vec,
+      ws_ptr<DeviceStatus>(ws, L.status));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_token_cluster(const smoe_desc& d, const int32_t* idx, const int32_t* emap,
                                  int32_t* cluster, void* ws, cudaStream_t s) {
   WsLayout L;

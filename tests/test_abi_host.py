@@ -132,6 +132,34 @@ def test_newer_entry_points_validate_on_the_host(lib):
     assert lib.smoe_combine(D, 16, 16, 16, None, None, 256, n, None) == -1
 
 
+def test_ffn_gather_validates_on_the_host(lib):
+    """smoe_expert_ffn_gather rejects missing or misaligned pointers before any CUDA call."""
+    d = base_desc()
+    n = B.workspace_size(d)
+    D = ctypes.byref(d)
+    # smoe_expert_ffn_gather(desc, x_src, row_slot, x, x_disp, expert_off, w1, w3, w2, y_disp,
+    #                        y_shared, ws, ws_bytes, stream)
+    assert lib.smoe_expert_ffn_gather(D, 16, None, None, 16, 16, 16, 16, 16, 16, None, 256, n,
+                                      None) == -1
+    assert lib.smoe_expert_ffn_gather(D, 16, 16 + 4, None, 16, 16, 16, 16, 16, 16, None, 256, n,
+                                      None) == -3
+    assert lib.smoe_expert_ffn_gather(D, 16, 16, None, 16, 16, 16, 16, 16, 16, None, 256, 16,
+                                      None) == -4
+
+
+def test_ffn_gather_fused_query(lib):
+    """The row copy runs inside the up GEMM only on bf16 two-SM tiles with F <= 1024: of
+    the workloads, the Qwen3-shaped layer (F = 768, 1024 rows per expert)."""
+    fused = {name: B.smoe_expert_ffn_gather_fused(B.desc_from_config(cfg))
+             for name, cfg in synth.CONFIGS.items()}
+    assert fused == {name: name == "qwen3_foe" for name in synth.CONFIGS}, fused
+    assert B.smoe_expert_ffn_gather_fused(base_desc(T=1024, E=8, K=2, F=1024))
+    assert not B.smoe_expert_ffn_gather_fused(base_desc(T=1024, E=8, K=2, F=1088))
+    assert not B.smoe_expert_ffn_gather_fused(base_desc(T=1023, E=8, K=2, F=256))  # < 256 rows
+    assert not B.smoe_expert_ffn_gather_fused(base_desc(T=1024, E=8, K=2, F=256, dtype="f32"))
+    assert not B.smoe_expert_ffn_gather_fused(base_desc(K=9))                     # invalid
+
+
 def test_prefetch_rejects_d_above_8192(lib):
     d = base_desc(d=8200)
     n = B.workspace_size(d)

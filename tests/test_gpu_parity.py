@@ -247,6 +247,100 @@ def test_dispatch(name, T):
     assert torch.equal(xd, c.x[torch.as_tensor(r_rt, device="cuda").long()])
 
 
+GATHER_CASES = [("tiny_fp32", 37), ("mixtral", 1001), ("dsv2_prefill", 1537), ("dsv2_decode", None),
+                ("qwen3_foe", 3001), ("mixtral", None), ("qwen3_foe", None)]
+
+
+@pytest.mark.parametrize("name,T", GATHER_CASES, ids=[f"{n}-T{t or 'full'}" for n, t in GATHER_CASES])
+def test_expert_ffn_gather(name, T):
+    """smoe_expert_ffn_gather (the dispatch's row copy inside the up GEMM on two-SM tiles,
+    a copy launch before the FFN otherwise) writes the same X_disp rows and, bit for bit,
+    the same expert outputs as smoe_dispatch's rows followed by smoe_expert_ffn, also in
+    place (X_disp and Y_disp one buffer); a bad row index gives a zero row and a data
+    error."""
+    c = get_case(name, T)
+    cfg = c.cfg
+    desc = smoe.desc_from_config(cfg)
+    ws = smoe.workspace(desc)
+    logits, idx, w = run_route(c, desc, ws)
+    pred, perm, off, xs = run_shuffle(c, desc, ws)
+    TK = cfg.T * cfg.K
+    eo, pr, rt, rs = i32(cfg.E + 1), i32(cfg.T, cfg.K), i32(TK), i32(TK)
+    xd = torch.empty(TK, cfg.d, dtype=c.x.dtype, device="cuda")
+    smoe.smoe_dispatch(desc, idx, eo, pr, rt, ws, shuf_perm=perm, x_src=xs, x_disp=xd, row_slot=rs)
+    yd = torch.empty_like(xd)
+
+    def shared():
+        return (torch.empty(cfg.n_shared, cfg.T, cfg.d, dtype=c.x.dtype, device="cuda")
+                if cfg.n_shared else None)
+
+    ysh = shared()
+    smoe.smoe_expert_ffn(desc, xd, eo, c.w1, c.w3, c.w2, yd, ws, x=c.x, y_shared=ysh)
+    xd2, yd2, ysh2 = torch.full_like(xd, 3.0), torch.full_like(xd, 5.0), shared()
+    smoe.smoe_expert_ffn_gather(desc, xs, rs, xd2, eo, c.w1, c.w3, c.w2, yd2, ws, x=c.x,
+                                y_shared=ysh2)
+    smoe.smoe_get_status(ws)
+    assert torch.equal(xd2, xd)
+    assert torch.equal(yd2, yd)
+    if ysh is not None:
+        assert torch.equal(ysh2, ysh)
+    buf = torch.full_like(xd, 7.0)
+    smoe.smoe_expert_ffn_gather(desc, xs, rs, buf, eo, c.w1, c.w3, c.w2, buf, ws, x=c.x,
+                                y_shared=ysh2)
+    smoe.smoe_get_status(ws)
+    assert torch.equal(buf, yd)
+    bad = rs.clone()
+    bad[TK // 2] = cfg.T + 5
+    xd3 = torch.full_like(xd, 3.0)
+    smoe.smoe_expert_ffn_gather(desc, xs, bad, xd3, eo, c.w1, c.w3, c.w2, yd2, ws, x=c.x,
+                                y_shared=ysh2)
+    with pytest.raises(smoe.SmoeError):
+        smoe.smoe_get_status(ws)
+    assert (xd3[TK // 2] == 0).all()
+    keep = torch.ones(TK, dtype=torch.bool, device="cuda")
+    keep[TK // 2] = False
+    assert torch.equal(xd3[keep], xd[keep])
+
+
+@pytest.mark.parametrize("d,F,counts,S", [
+    (2048, 768, [700, 1300, 0, 1024, 97, 3001, 256, 1], 0),
+    (5120, 512, [300, 0, 513, 129, 1100], 1),
+    (256, 256, [64, 300, 450, 0, 129, 128, 513, 500], 1),
+    (384, 704, [1, 2000, 255, 700], 0)],
+    ids=["d2048-chunk4", "d5120-chunk1", "d256-chunk32", "d384-chunk16"])
+def test_expert_ffn_gather_in_gemm(d, F, counts, S):
+    """The in-GEMM row copy (bf16 two-SM tiles, F <= 1024) with chunks of 1 to 32 rows,
+    ragged and empty expert segments and shared experts: X_disp and the expert outputs
+    equal a torch row gather followed by smoe_expert_ffn, bit for bit."""
+    E, K = len(counts), 2
+    TK = sum(counts)
+    T = (TK + K - 1) // K
+    desc = smoe.make_desc(T, d, E, K, 1, F, S, 2, 100, "bf16")
+    assert smoe.smoe_expert_ffn_gather_fused(desc)
+    g = torch.Generator(device="cuda").manual_seed(d + F)
+    x = torch.randn(T, d, generator=g, device="cuda").to(torch.bfloat16)
+    w1 = (torch.randn(E + S, F, d, generator=g, device="cuda") / d ** 0.5).to(torch.bfloat16)
+    w3 = (torch.randn(E + S, F, d, generator=g, device="cuda") / d ** 0.5).to(torch.bfloat16)
+    w2 = (torch.randn(E + S, d, F, generator=g, device="cuda") / F ** 0.5).to(torch.bfloat16)
+    slots = torch.randint(0, T, (T * K,), generator=g, device="cuda", dtype=torch.int32)
+    slots[TK:] = 0
+    eo = torch.as_tensor(np.concatenate([[0], np.cumsum(counts)]).astype(np.int32), device="cuda")
+    ws = smoe.workspace(desc)
+    xd_ref = x[slots.long()]
+    xd_ref[TK:] = 0
+    y_ref = torch.empty_like(xd_ref)
+    ysh_ref = torch.empty(S, T, d, dtype=torch.bfloat16, device="cuda") if S else None
+    smoe.smoe_expert_ffn(desc, xd_ref, eo, w1, w3, w2, y_ref, ws, x=x, y_shared=ysh_ref)
+    xd, y = torch.zeros_like(xd_ref), torch.full_like(xd_ref, 9.0)
+    ysh = torch.empty_like(ysh_ref) if S else None
+    smoe.smoe_expert_ffn_gather(desc, x, slots, xd, eo, w1, w3, w2, y, ws, x=x, y_shared=ysh)
+    smoe.smoe_get_status(ws)
+    assert torch.equal(xd[:TK], xd_ref[:TK])
+    assert torch.equal(y[:TK], y_ref[:TK])
+    if S:
+        assert torch.equal(ysh, ysh_ref)
+
+
 @pytest.mark.parametrize("name,T", CASES, ids=IDS)
 def test_expert_ffn_and_combine(name, T):
     c = get_case(name, T)
