@@ -14,8 +14,10 @@ constexpr int kThreads = 128;
 constexpr int kBatch = 8;  // row loads in flight per thread
 
 // U vectors per thread and iteration, kBatch / U rows of each loaded before the first
-// accumulation: with K = 2, U = 4 keeps 8 loads in flight per thread instead of 2.
-template <typename TE, int U>
+// accumulation: with K = 2, U = 4 keeps 8 loads in flight per thread instead of 2. With
+// shared experts one batch spans the routed and the shared rows (one round trip instead
+// of two per vector when K + S <= 8); without, the plain routed loop is cheaper.
+template <typename TE, int U, bool SH>
 __global__ void __launch_bounds__(kThreads)
 combine_kernel(const uint4* __restrict__ y_disp, const int32_t* __restrict__ pair_row,
                const float* __restrict__ w, const uint4* __restrict__ y_sh, uint4* __restrict__ y,
@@ -41,52 +43,73 @@ combine_kernel(const uint4* __restrict__ y_disp, const int32_t* __restrict__ pai
     for (int uu = 0; uu < U; ++uu)
 #pragma unroll
       for (int i = 0; i < V; ++i) acc[uu][i] = 0.0f;
-    // batches of KB rows: all of a batch's loads (for the U vectors) are issued before
-    // the first accumulation, which still runs in the order k = 0, 1, ... per vector
-    for (int k0 = 0; k0 < K; k0 += KB) {
-      uint4 u[U][KB];
+    if constexpr (!SH) {
+      // batches of KB rows: all of a batch's loads (for the U vectors) are issued before
+      // the first accumulation, which still runs in the order k = 0, 1, ... per vector
+      for (int k0 = 0; k0 < K; k0 += KB) {
+        uint4 u[U][KB];
 #pragma unroll
-      for (int uu = 0; uu < U; ++uu) {
-        const int v = v0 + uu * kThreads;
+        for (int uu = 0; uu < U; ++uu) {
+          const int v = v0 + uu * kThreads;
 #pragma unroll
-        for (int b = 0; b < KB; ++b) {
-          const int r = k0 + b < K ? s_row[k0 + b] : -1;
-          u[uu][b] = (r >= 0 && v < nvec) ? __ldg(y_disp + (size_t)r * nvec + v)
-                                          : make_uint4(0, 0, 0, 0);
+          for (int b = 0; b < KB; ++b) {
+            const int r = k0 + b < K ? s_row[k0 + b] : -1;
+            u[uu][b] = (r >= 0 && v < nvec) ? __ldg(y_disp + (size_t)r * nvec + v)
+                                            : make_uint4(0, 0, 0, 0);
+          }
+        }
+#pragma unroll
+        for (int uu = 0; uu < U; ++uu) {
+#pragma unroll
+          for (int b = 0; b < KB; ++b) {
+            if (k0 + b >= K || s_row[k0 + b] < 0) continue;
+            float f[V];
+            unpack16(u[uu][b], f, tag);
+            const float wk = s_w[k0 + b];
+#pragma unroll
+            for (int i = 0; i < V; ++i) acc[uu][i] = fmaf(wk, f[i], acc[uu][i]);
+          }
         }
       }
+    } else {
+      // batches of KB of the K + S rows (routed rows k = 0..K-1, then shared rows): all of a
+      // batch's loads (for the U vectors) are issued before the first accumulation, which
+      // still runs in the order k = 0..K-1 (weighted) then j = 0..S-1
+      for (int q0 = 0; q0 < K + S; q0 += KB) {
+        uint4 u[U][KB];
 #pragma unroll
-      for (int uu = 0; uu < U; ++uu) {
+        for (int uu = 0; uu < U; ++uu) {
+          const int v = v0 + uu * kThreads;
 #pragma unroll
-        for (int b = 0; b < KB; ++b) {
-          if (k0 + b >= K || s_row[k0 + b] < 0) continue;
-          float f[V];
-          unpack16(u[uu][b], f, tag);
-          const float wk = s_w[k0 + b];
-#pragma unroll
-          for (int i = 0; i < V; ++i) acc[uu][i] = fmaf(wk, f[i], acc[uu][i]);
+          for (int b = 0; b < KB; ++b) {
+            const int q = q0 + b;
+            const uint4* src = nullptr;
+            if (q < K) {
+              const int r = s_row[q];
+              if (r >= 0) src = y_disp + (size_t)r * nvec;
+            } else if (q < K + S) {
+              src = y_sh + ((size_t)(q - K) * T + t) * nvec;
+            }
+            u[uu][b] = (src != nullptr && v < nvec) ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+          }
         }
-      }
-    }
-    for (int j0 = 0; j0 < S; j0 += KB) {
-      uint4 u[U][KB];
 #pragma unroll
-      for (int uu = 0; uu < U; ++uu) {
-        const int v = v0 + uu * kThreads;
+        for (int uu = 0; uu < U; ++uu) {
 #pragma unroll
-        for (int b = 0; b < KB; ++b)
-          u[uu][b] = (j0 + b < S && v < nvec) ? __ldg(y_sh + ((size_t)(j0 + b) * T + t) * nvec + v)
-                                              : make_uint4(0, 0, 0, 0);
-      }
+          for (int b = 0; b < KB; ++b) {
+            const int q = q0 + b;
+            if (q >= K + S || (q < K && s_row[q] < 0)) continue;
+            float f[V];
+            unpack16(u[uu][b], f, tag);
+            if (q < K) {
+              const float wk = s_w[q];
 #pragma unroll
-      for (int uu = 0; uu < U; ++uu) {
+              for (int i = 0; i < V; ++i) acc[uu][i] = fmaf(wk, f[i], acc[uu][i]);
+            } else {
 #pragma unroll
-        for (int b = 0; b < KB; ++b) {
-          if (j0 + b >= S) continue;
-          float f[V];
-          unpack16(u[uu][b], f, tag);
-#pragma unroll
-          for (int i = 0; i < V; ++i) acc[uu][i] += f[i];
+              for (int i = 0; i < V; ++i) acc[uu][i] += f[i];
+            }
+          }
         }
       }
     }
@@ -106,15 +129,23 @@ cudaError_t launch_combine_t(const smoe_desc& d, const void* y_disp, const int32
   const uint4* ys = static_cast<const uint4*>(y_sh);
   uint4* yo = static_cast<uint4*>(y);
   const int rows = d.T * d.K;
-  if (d.K + S <= 2)
-    SMOE_LAUNCH((combine_kernel<TE, 4>), d.T, kThreads, 0, s, yd, pair_row, w, ys, yo, d.T, d.K,
-                S, nvec, rows, st);
-  else if (d.K + S <= 4)
-    SMOE_LAUNCH((combine_kernel<TE, 2>), d.T, kThreads, 0, s, yd, pair_row, w, ys, yo, d.T, d.K,
-                S, nvec, rows, st);
-  else
-    SMOE_LAUNCH((combine_kernel<TE, 1>), d.T, kThreads, 0, s, yd, pair_row, w, ys, yo, d.T, d.K,
-                S, nvec, rows, st);
+  if (S > 0) {  // K + S > 2 always holds here (K >= 1)
+    if (d.K + S <= 4)
+      SMOE_LAUNCH((combine_kernel<TE, 2, true>), d.T, kThreads, 0, s, yd, pair_row, w, ys, yo, d.T,
+                  d.K, S, nvec, rows, st);
+    else
+      SMOE_LAUNCH((combine_kernel<TE, 1, true>), d.T, kThreads, 0, s, yd, pair_row, w, ys, yo, d.T,
+                  d.K, S, nvec, rows, st);
+  } else if (d.K <= 2) {
+    SMOE_LAUNCH((combine_kernel<TE, 4, false>), d.T, kThreads, 0, s, yd, pair_row, w, ys, yo, d.T,
+                d.K, S, nvec, rows, st);
+  } else if (d.K <= 4) {
+    SMOE_LAUNCH((combine_kernel<TE, 2, false>), d.T, kThreads, 0, s, yd, pair_row, w, ys, yo, d.T,
+                d.K, S, nvec, rows, st);
+  } else {
+    SMOE_LAUNCH((combine_kernel<TE, 1, false>), d.T, kThreads, 0, s, yd, pair_row, w, ys, yo, d.T,
+                d.K, S, nvec, rows, st);
+  }
   return cudaGetLastError();
 }
 
