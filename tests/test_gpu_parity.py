@@ -121,7 +121,9 @@ def test_route_selection_ties(E, K, H, renorm):
                                        (650, 320, 99, 3, 3),
                                        (64, 1024, 8, 8, 1), (2000, 256, 256, 16, 2),
                                        (129, 512, 256, 8, 8), (700, 256, 64, 8, 8),
-                                       (64, 5120, 160, 6, 1)])
+                                       (64, 5120, 160, 6, 1), (1, 64, 1, 1, 1),
+                                       (5, 64, 256, 16, 16), (130, 64, 129, 16, 1),
+                                       (33, 4096, 40, 8, 4)])
 @pytest.mark.parametrize("renorm", [0, 1])
 def test_route_fused_gemm_ties(T, d, E, K, H, renorm):
     """The bf16 gate GEMM with the selection in its epilogue (E <= 256, K <= 8 lanes per
