@@ -568,8 +568,11 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
 // selection read consecutive words.
 constexpr int kMaxFusedStages = 16;
 // warps 0-7: producer, MMA, TMEM allocation, idle, 4 x TMEM readers; warps 8-15 join
-// the reduction and the selection
+// the reduction and the selection. With more row tiles than SMs the kernel runs 256
+// threads and a 3-stage ring instead, so that two CTAs share an SM and one's selection
+// overlaps the other's GEMM.
 constexpr int kFusedThreads = 512;
+constexpr int kFusedThreadsCompact = 256;
 
 struct FusedRouteArgs {
   DeviceStatus* st;
@@ -581,6 +584,7 @@ struct FusedRouteArgs {
   uint32_t idesc, b_stage, tmem_cols;
   uint32_t sum_off;   // byte offset of the summed-logit buffer (CS > 1)
   int stages;         // operand ring depth
+  int threads;        // kFusedThreads, or kFusedThreadsCompact with more tiles than SMs
 };
 
 // byte offset of (row r, column c) in a logit buffer of the given pitch (floats)
@@ -729,7 +733,7 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
       sr0 = 0;
     }
     const int nq = ncol >> 2;
-    for (int item = threadIdx.x; item < R * nq; item += kFusedThreads) {
+    for (int item = threadIdx.x; item < R * nq; item += (int)blockDim.x) {
       const int rr = item / nq, c4 = item % nq;
       float4 a;
       if (CS == 1) {
@@ -762,7 +766,7 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
     __syncthreads();
     // ------------------------------------------------------------------ selection
     const int j = threadIdx.x & (L - 1);
-    for (int rr0 = 0; rr0 < R; rr0 += kFusedThreads / L) {
+    for (int rr0 = 0; rr0 < R; rr0 += (int)blockDim.x / L) {
       const int rr = rr0 + (int)threadIdx.x / L;
       const bool in = rr < R;
       float v[kPer];
@@ -813,13 +817,11 @@ int device_sms() {
   return n > 0 ? n : 152;
 }
 
-// The fused kernel takes bf16 layers with E <= 256 (one MMA of N = E rounded up to 16),
-// K no larger than the lanes per token of its selection (8 for E <= 128, else 16), and
-// row tiles that fit one wave: with more tiles than SMs its one-CTA-per-SM footprint
-// serialises the second wave, and the two-launch path (measured faster there) is used.
+// The fused kernel takes bf16 layers with E <= 256 (one MMA of N = E rounded up to 16)
+// and K no larger than the lanes per token of its selection (8 for E <= 128, else 16).
 bool fused_route_ok(const smoe_desc& d, int rows) {
-  return d.dtype == SMOE_BF16 && d.E <= 256 && d.K <= (d.E <= 128 ? 8 : 16) &&
-         ceil_div(rows, 128) <= device_sms();
+  (void)rows;
+  return d.dtype == SMOE_BF16 && d.E <= 256 && d.K <= (d.E <= 128 ? 8 : 16);
 }
 
 // Cluster size: the largest power of two of k-splits that keeps one wave of clusters on
@@ -841,7 +843,7 @@ cudaError_t launch_fused(const CUtensorMap& tX, const CUtensorMap& tW, const Fus
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(tiles * a.CS);
-  cfg.blockDim = dim3(kFusedThreads);
+  cfg.blockDim = dim3(a.threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -887,8 +889,11 @@ cudaError_t launch_route_fused(const smoe_desc& d, int rows, const void* x, cons
   const uint32_t stage = kGateA + a.b_stage;
   const uint32_t budget = 227u * 1024u - 1024u - 8u * (2u * kMaxFusedStages + 2u) - 16u;
   const int kb_split = ceil_div(a.nkb, a.CS);
+  const bool compact = ceil_div(rows, 128) > device_sms();
+  a.threads = compact ? kFusedThreadsCompact : kFusedThreads;
   a.stages = (int)std::min<uint32_t>(std::min<uint32_t>(budget / stage, kMaxFusedStages),
                                      (uint32_t)std::max(kb_split, 2));
+  if (compact) a.stages = std::min(a.stages, 3);
   const uint32_t ring = (uint32_t)a.stages * stage;
   const uint32_t pitch = ncol + 4u;  // floats per row of a logit buffer
   a.sum_off = pitch * 512u;

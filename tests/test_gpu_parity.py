@@ -123,12 +123,14 @@ def test_route_selection_ties(E, K, H, renorm):
                                        (129, 512, 256, 8, 8), (700, 256, 64, 8, 8),
                                        (64, 5120, 160, 6, 1), (1, 64, 1, 1, 1),
                                        (5, 64, 256, 16, 16), (130, 64, 129, 16, 1),
-                                       (33, 4096, 40, 8, 4)])
+                                       (33, 4096, 40, 8, 4), (20000, 128, 64, 8, 2),
+                                       (40000, 64, 128, 8, 8)])
 @pytest.mark.parametrize("renorm", [0, 1])
 def test_route_fused_gemm_ties(T, d, E, K, H, renorm):
     """The bf16 gate GEMM with the selection in its epilogue (E <= 256, K <= 8 lanes per
-    token for E <= 128, else 16, at most one 128-row tile per SM), split over clusters of
-    1, 2, 4 or 8 CTAs; E = 16 with K = 16 takes the two-launch path. x and W_g in {-1, 0, 1} make every logit an exact
+    token for E <= 128, else 16), split over clusters of 1, 2, 4 or 8 CTAs, and with more
+    128-row tiles than SMs in its compact form (256 threads, two CTAs per SM); E = 16 with
+    K = 16 takes the two-launch path. x and W_g in {-1, 0, 1} make every logit an exact
     small integer, so the exported logits must equal the exact products and many of them
     tie (the lower index must win); picks and weights are then checked against the
     oracle's selection on those logits."""
