@@ -931,8 +931,15 @@ int route_splits(const smoe_desc& d, int rows) {
 cudaError_t launch_route(const smoe_desc& d, int rows, const void* x, const void* w_gate,
                          const float* logits_in, float* logits_out, int32_t* topk_idx,
                          float* topk_w, void* ws, cudaStream_t s, RouteSplitOut so) {
-  if (!logits_in && fused_route_ok(d, rows))
-    return launch_route_fused(d, rows, x, w_gate, logits_out, topk_idx, topk_w, ws, s, so);
+  if (!logits_in && fused_route_ok(d, rows)) {
+    const cudaError_t e =
+        launch_route_fused(d, rows, x, w_gate, logits_out, topk_idx, topk_w, ws, s, so);
+    if (e == cudaSuccess) return e;
+    // a cluster shape the device cannot schedule (e.g. a partitioned GPU) is rejected at
+    // launch, before anything runs: take the two-launch path instead
+    if (e != cudaErrorInvalidClusterSize && e != cudaErrorLaunchOutOfResources) return e;
+    (void)cudaGetLastError();
+  }
   const float* part = logits_in;
   int KS = 1;
   if (!logits_in) {
