@@ -346,8 +346,8 @@ scatter_kernel(const int32_t* __restrict__ bucket, int n, int B, int ntiles, int
 }
 
 // ------------------------------------------------------------------ row gather
-// dst[r] = src[map[r]] for 16-byte-aligned rows; one warp per row, four 16-byte
-// loads in flight per lane.
+// dst[r] = src[map[r]] for 16-byte-aligned rows; one warp per row, eight 16-byte
+// loads in flight per lane (four for the last part of a row).
 __global__ void __launch_bounds__(kThreads)
 gather_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
                    const int32_t* __restrict__ map, int nrows, int nsrc, int vec_per_row,
@@ -366,6 +366,13 @@ gather_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
     }
     const uint4* in = src + (size_t)s * vec_per_row;
     int v = lane;
+    for (; v + 224 < vec_per_row; v += 256) {
+      uint4 t[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) t[u] = __ldg(in + v + 32 * u);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) out[v + 32 * u] = t[u];
+    }
     for (; v + 96 < vec_per_row; v += 128) {
       const uint4 a = __ldg(in + v), b = __ldg(in + v + 32), c = __ldg(in + v + 64),
                   d = __ldg(in + v + 96);
