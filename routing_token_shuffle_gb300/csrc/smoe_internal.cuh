@@ -117,7 +117,8 @@ extern thread_local unsigned long long g_kernel_launches;
 #define SMOE_COUNT_LAUNCH(n) (::smoe::g_kernel_launches += (n))
 
 // ---------------------------------------------------------------- dependent launch
-// Every library kernel is launched with programmatic stream serialisation and starts with
+// Every library kernel but the combine (launch_k_serial) is launched with programmatic
+// stream serialisation and starts with
 // pdl_wait() (griddepcontrol.wait: the previous kernel in the stream has completed and its
 // writes are visible) before touching global memory, then pdl_trigger() so that the next
 // kernel's CTAs may be scheduled while this grid drains. Without a programmatic
@@ -144,10 +145,37 @@ inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_
   return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
 }
 
+// A kernel that follows a long persistent GEMM: launched programmatically, its CTAs
+// become resident beside the GEMM's (whose CTAs all start at once) and wait there for
+// the whole GEMM, which slowed the Qwen3-shaped step by ~24 us. Plain stream order.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k_serial(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                   cudaStream_t s, Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  SMOE_COUNT_LAUNCH(1);
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 #define SMOE_LAUNCH(kern, grid, block, smem, stream, ...)                              \
   do {                                                                                 \
     cudaError_t le_ = ::smoe::launch_k(kern, dim3(grid), dim3(block), smem, stream,     \
                                        __VA_ARGS__);                                   \
+    if (le_ != cudaSuccess) return le_;                                                \
+  } while (0)
+
+#define SMOE_LAUNCH_SERIAL(kern, grid, block, smem, stream, ...)                       \
+  do {                                                                                 \
+    cudaError_t le_ = ::smoe::launch_k_serial(kern, dim3(grid), dim3(block), smem,      \
+                                              stream, __VA_ARGS__);                    \
     if (le_ != cudaSuccess) return le_;                                                \
   } while (0)
 
