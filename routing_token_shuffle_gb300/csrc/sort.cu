@@ -422,45 +422,6 @@ __device__ __forceinline__ int foe_source(int t, int h, int G, int H) {
   return H >= G ? (h * G) / H : h * (G / H) + (t % (G / H));
 }
 
-// Local, contiguous-split and best-partition counts of token t (the LAR of "Speculative
-// MoE" §2 / §7, with the FoE grouped source rule when src_part is NULL).
-__device__ __forceinline__ void lar_token(int t, const int32_t* __restrict__ idx,
-                                         const int32_t* __restrict__ src_part,
-                                         const int* s_map, int T, int K, int E, int P, int H,
-                                         unsigned long long& loc, unsigned long long& base,
-                                         unsigned long long& mx, DeviceStatus* st) {
-  const int kh = K / H;
-  int src = -1;
-  if (src_part) {
-    src = src_part[t];
-    if ((unsigned)src >= (unsigned)P) {
-      record_error(st, kStatusData, kBadSrcPart, t);
-      src = -1;
-    }
-  }
-  const int bsrc = (int)(((long long)t * P) / T);
-  const int32_t* row = idx + (size_t)t * K;
-  int best = 0;
-  for (int k = 0; k < K; ++k) {
-    const int e = row[k];
-    int dst = -1;
-    if ((unsigned)e < (unsigned)E) dst = s_map[e];
-    else record_error(st, kStatusData, kBadTopkIdx, (long long)t * K + k);
-    const int sp = src_part ? src : foe_source(t, k / kh, P, H);
-    loc += (dst >= 0 && dst == sp);
-    base += (dst >= 0 && dst == bsrc);
-    if (dst >= 0) {
-      int c = 0;
-      for (int k2 = 0; k2 < K; ++k2) {
-        const int e2 = row[k2];
-        c += ((unsigned)e2 < (unsigned)E && s_map[e2] == dst);
-      }
-      best = max(best, c);
-    }
-  }
-  mx += best;
-}
-
 __global__ void __launch_bounds__(kThreads)
 lar_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ src_part,
            const int32_t* __restrict__ emap, int T, int K, int E, int P, int H,
@@ -477,8 +438,38 @@ lar_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ src_part
   }
   __syncthreads();
   unsigned long long loc = 0, base = 0, mx = 0;
-  for (int t = blockIdx.x * kThreads + tid; t < T; t += gridDim.x * kThreads)
-    lar_token(t, idx, src_part, s_map, T, K, E, P, H, loc, base, mx, st);
+  const int kh = K / H;
+  for (int t = blockIdx.x * kThreads + tid; t < T; t += gridDim.x * kThreads) {
+    int src = -1;
+    if (src_part) {
+      src = src_part[t];
+      if ((unsigned)src >= (unsigned)P) {
+        record_error(st, kStatusData, kBadSrcPart, t);
+        src = -1;
+      }
+    }
+    const int bsrc = (int)(((long long)t * P) / T);
+    const int32_t* row = idx + (size_t)t * K;
+    int best = 0;
+    for (int k = 0; k < K; ++k) {
+      const int e = row[k];
+      int dst = -1;
+      if ((unsigned)e < (unsigned)E) dst = s_map[e];
+      else record_error(st, kStatusData, kBadTopkIdx, (long long)t * K + k);
+      const int sp = src_part ? src : foe_source(t, k / kh, P, H);
+      loc += (dst >= 0 && dst == sp);
+      base += (dst >= 0 && dst == bsrc);
+      if (dst >= 0) {
+        int c = 0;
+        for (int k2 = 0; k2 < K; ++k2) {
+          const int e2 = row[k2];
+          c += ((unsigned)e2 < (unsigned)E && s_map[e2] == dst);
+        }
+        best = max(best, c);
+      }
+    }
+    mx += best;
+  }
 #pragma unroll
   for (int off = 16; off; off >>= 1) {
     loc += __shfl_xor_sync(0xffffffffu, loc, off);
@@ -494,48 +485,6 @@ lar_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ src_part
     atomicAdd(counts + slot, v);
   }
   if (blockIdx.x == 0 && tid == 0) atomicAdd(counts + 1, (unsigned long long)T * K);
-}
-
-// One CTA of 1024 threads when the work is small (T K^2 <= kLarBlockWork: a token's best
-// partition compares its K picks pairwise): the counts are written, not added, so the
-// call needs no clearing of `counts` before it. Measured: Mixtral shape 9.0 -> 7.7 us;
-// at T K^2 = 295K (DeepSeek-V2) one CTA took 31 us against 8.8 for the grid.
-constexpr int kLarBlockThreads = 1024;
-constexpr long long kLarBlockWork = 32768;
-
-__global__ void __launch_bounds__(kLarBlockThreads)
-lar_block_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ src_part,
-                 const int32_t* __restrict__ emap, int T, int K, int E, int P, int H,
-                 unsigned long long* __restrict__ counts, DeviceStatus* st) {
-  pdl_wait_and_trigger();
-  constexpr int kW = kLarBlockThreads / 32;
-  __shared__ int s_map[kMaxBuckets];
-  __shared__ unsigned long long s_red[3][kW];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int e = tid; e < E; e += kLarBlockThreads) {
-    const int p = emap[e];
-    const bool ok = (unsigned)p < (unsigned)P;
-    if (!ok) record_error(st, kStatusData, kBadExpertPart, e);
-    s_map[e] = ok ? p : -1;
-  }
-  __syncthreads();
-  unsigned long long loc = 0, base = 0, mx = 0;
-  for (int t = tid; t < T; t += kLarBlockThreads)
-    lar_token(t, idx, src_part, s_map, T, K, E, P, H, loc, base, mx, st);
-#pragma unroll
-  for (int off = 16; off; off >>= 1) {
-    loc += __shfl_xor_sync(0xffffffffu, loc, off);
-    base += __shfl_xor_sync(0xffffffffu, base, off);
-    mx += __shfl_xor_sync(0xffffffffu, mx, off);
-  }
-  if (lane == 0) { s_red[0][warp] = loc; s_red[1][warp] = base; s_red[2][warp] = mx; }
-  __syncthreads();
-  if (tid < 3) {
-    unsigned long long v = 0;
-    for (int w = 0; w < kW; ++w) v += s_red[tid][w];
-    counts[tid == 0 ? 0 : (tid == 1 ? 2 : 3)] = v;
-  }
-  if (tid == 3) counts[1] = (unsigned long long)T * K;
 }
 
 int grid_for_rows(long long nrows) {
@@ -661,11 +610,6 @@ cudaError_t launch_lar(const smoe_desc& d, const int32_t* idx, const int32_t* sr
   WsLayout L;
   ws_layout(d, &L);
   DeviceStatus* st = ws_ptr<DeviceStatus>(ws, L.status);
-  if ((long long)d.T * d.K * d.K <= kLarBlockWork) {
-    SMOE_LAUNCH(lar_block_kernel, 1, kLarBlockThreads, 0, s, idx, src_part, emap, d.T, d.K, d.E,
-        d.P, d.H, counts, st);
-    return cudaGetLastError();
-  }
   cudaError_t e = cudaMemsetAsync(counts, 0, 4 * sizeof(unsigned long long), s);
   if (e != cudaSuccess) return e;
   const int grid = std::max(1, std::min(ceil_div(d.T, kThreads), 1024));
