@@ -8,6 +8,7 @@
  *   local activation rate alpha                     -> smoe_lar
  *   permute pairs into per-expert contiguous rows   -> smoe_dispatch
  *   grouped SwiGLU expert FFN                       -> smoe_expert_ffn
+ *   dispatch's row copy + expert FFN in one call    -> smoe_expert_ffn_gather
  *   weighted combine back into token order          -> smoe_combine
  *   all of the above in one call                    -> smoe_layer_forward
  *   next-layer route predictor q = LN(d + r)        -> smoe_prefetch_predict
