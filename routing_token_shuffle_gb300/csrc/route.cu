@@ -819,8 +819,7 @@ int device_sms() {
 
 // The fused kernel takes bf16 layers with E <= 256 (one MMA of N = E rounded up to 16)
 // and K no larger than the lanes per token of its selection (8 for E <= 128, else 16).
-bool fused_route_ok(const smoe_desc& d, int rows) {
-  (void)rows;
+bool fused_route_ok(const smoe_desc& d) {
   return d.dtype == SMOE_BF16 && d.E <= 256 && d.K <= (d.E <= 128 ? 8 : 16);
 }
 
@@ -931,7 +930,7 @@ int route_splits(const smoe_desc& d, int rows) {
 cudaError_t launch_route(const smoe_desc& d, int rows, const void* x, const void* w_gate,
                          const float* logits_in, float* logits_out, int32_t* topk_idx,
                          float* topk_w, void* ws, cudaStream_t s, RouteSplitOut so) {
-  if (!logits_in && fused_route_ok(d, rows)) {
+  if (!logits_in && fused_route_ok(d)) {
     const cudaError_t e =
         launch_route_fused(d, rows, x, w_gate, logits_out, topk_idx, topk_w, ws, s, so);
     if (e == cudaSuccess) return e;
