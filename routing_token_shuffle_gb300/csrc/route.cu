@@ -6,8 +6,10 @@
 // all experts taken at the selected indices.
 //
 // bf16 layers: the gate GEMM runs on tcgen05 (M = 128 token rows, N = E rounded up to
-// 16, K split over KS CTAs so that even 32 row tiles fill the GPU); each split writes
-// fp32 partial logits, and the selection kernel adds the KS partials in split order.
+// 16, K split over the CTAs of a cluster, or over KS CTAs in the two-launch path). With
+// E <= 256 and K no larger than the lanes per token, route_fused_kernel reduces the split
+// partials in distributed shared memory and selects in the same launch; otherwise each
+// split writes fp32 partial logits and a selection kernel adds them in split order.
 // fp32 layers keep an exact fp32-FMA gate GEMM: the tensor cores would round the
 // operands to tf32 and move logits by ~1e-3, enough to flip routing decisions.
 //
@@ -554,12 +556,13 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
 // gate_tc_kernel. Each rank's epilogue copies its partial logits into its own shared
 // memory (the operand ring is free once its MMAs have completed); a cluster barrier
 // (release / acquire) publishes them. Rank b then owns rows [b R, (b + 1) R), R = 128 /
-// CS: its 256 threads add the CS partials of those rows in rank order (the order in which
-// the select kernels add the splits of the two-launch path), reading the other ranks'
-// buffers through distributed shared memory, and select on the sums with L lanes per
-// token (select_sub_row: the same picks, order and weights as select_sub_kernel). Partial
-// logits never leave the chip, the reduction and the selection are spread over the
-// cluster, and CS is chosen so that one wave of clusters covers the SMs.
+// CS: its threads (512; 256 in the compact form) add the CS partials of those rows in
+// rank order (the order in which the select kernels add the splits of the two-launch
+// path), reading the other ranks' buffers through distributed shared memory, and select
+// on the sums with L lanes per token (select_sub_row / select_group1_row: the same picks,
+// order and weights as the select kernels). Partial logits never leave the chip, the
+// reduction and the selection are spread over the cluster, and CS is chosen so that one
+// wave of clusters covers the SMs.
 //
 // Shared-memory logit buffers (partials and sums) are row-major with a pitch of ncol + 4
 // floats (ncol = E_pad rounded up to 32): a warp storing one 16-byte quad per row for 32
