@@ -234,10 +234,12 @@ def test_lar_direct_count(T, E, K, P):
     assert got[0] <= got[3]        # alpha_sTS <= alpha_max
 
 
-def test_lar_foe_rule_direct_count():
-    rng = np.random.default_rng(11)
+@pytest.mark.parametrize("K", [2, 4])
+def test_lar_foe_rule_direct_count(K):
+    """H < G: copy (t, h) sits on h (G/H) + (t mod G/H); with K/H > 1 the group of slot
+    k is k // (K/H), not k mod H."""
+    rng = np.random.default_rng(11 + K)
     T, E, H, G = 40, 16, 2, 8
-    K = 2
     logits = rng.standard_normal((T, E)).astype(np.float32)
     idx = O.topk_select(logits, K, H=H)
     # group h spans partitions 4h..4h+3; its j-th expert is on 4h + (j mod 4)
@@ -245,6 +247,30 @@ def test_lar_foe_rule_direct_count():
     got = O.lar_counts(idx, emap, G, H).tolist()
     exp = direct_lar(idx, emap, G, H, lambda t, k: (k // (K // H)) * (G // H) + t % (G // H))
     assert got == exp
+
+
+@pytest.mark.parametrize("H,G,K", [(4, 2, 8), (4, 4, 8), (8, 2, 8)])
+def test_lar_foe_rule_direct_count_H_ge_G(H, G, K):
+    """H >= G: every copy for group h sits on floor(h G / H), checked on a random map."""
+    rng = np.random.default_rng(100 * H + G)
+    T, E = 30, 16
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    idx = O.topk_select(logits, K, H=H)
+    emap = rng.integers(0, G, size=E).astype(np.int32)
+    got = O.lar_counts(idx, emap, G, H).tolist()
+    exp = direct_lar(idx, emap, G, H, lambda t, k: ((k // (K // H)) * G) // H)
+    assert got == exp
+
+
+@pytest.mark.parametrize("H", [1, 2])
+def test_layer_alpha_counts_from_predicted_partition(H):
+    """The layer's alpha counts a routed pair as local when its expert sits on the
+    partition the token was shuffled to (its predicted partition)."""
+    x, ids, wg, w1, w3, w2, conf, emap = tiny_layer(seed=40 + H, T=60, E=8, K=4, H=H, P=4)
+    out = O.layer_forward(x, ids, wg, w1, w3, w2, conf, emap, K=4, H=H, P=4)
+    pred = out["pred"]
+    assert len(set(pred.tolist())) > 1
+    assert out["lar"].tolist() == direct_lar(out["idx"], emap, 4, H, lambda t, k: int(pred[t]))
 
 
 def test_lar_max_equals_sts_when_table_is_exact():
@@ -597,6 +623,18 @@ def test_speculative_execution_pins():
                      - O.swiglu_ffn(x[5:6], w1[old], w3[old], w2[old])[0])
     np.testing.assert_allclose(diff[5], exp, rtol=1e-10, atol=1e-12)
     assert dev2 > 0
+
+
+def test_speculative_execution_uses_the_predicted_weights():
+    """Same routes, predicted weights twice the true ones, no shared expert: the routed
+    output is linear in the weights, so y_spec = 2 y_true exactly and the deviation is 1."""
+    x, ids, wg, w1, w3, w2, conf, emap = tiny_layer(seed=32, E=8, K=2, S=0)
+    logits = O.gate_logits(x, wg)
+    idx = O.topk_select(logits, 2)
+    w = O.gate_weights(logits, idx)
+    y_spec, y_true, dev = O.speculative_execution(x, idx, 2.0 * w, idx, w, w1, w3, w2)
+    np.testing.assert_allclose(y_spec, 2.0 * y_true, rtol=1e-13, atol=0)
+    assert abs(dev - 1.0) < 1e-12
 
 
 # ------------------------------------------------- co-clustering (s-EG) ------
