@@ -98,10 +98,16 @@ def lib(path: str | None = None):
 
 
 def _ptr(t):
+    """A tensor's address, or a raw integer address passed through. Every buffer of the C
+    ABI is dense row-major, so a strided view (a transpose, a column slice, an expand)
+    is refused here instead of being read as if it were dense."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    if not t.is_contiguous():
+        raise ValueError(f"tensor of shape {tuple(t.shape)} and strides {t.stride()} is not "
+                         "contiguous; the C ABI takes dense row-major buffers (call .contiguous())")
     return t.data_ptr()
 
 

@@ -166,3 +166,20 @@ def test_prefetch_rejects_d_above_8192(lib):
     rc = lib.smoe_prefetch_predict(ctypes.byref(d), 16, 16, 16, 16, 16, 16, None, None, 16, 16,
                                    16, None, 256, n, None)
     assert rc == -2 and b"8192" in lib.smoe_last_error()
+
+
+def test_binding_refuses_strided_views(lib):
+    """The ABI takes dense row-major buffers: a transposed or column-sliced tensor is refused
+    by the binding before the C call, instead of being read as if it were dense."""
+    import torch
+    d = base_desc(T=16, d=64, E=8, K=2)
+    y_disp = torch.zeros(64, 32)                     # [d, T*K] storage, viewed transposed
+    pair_row = torch.zeros(16, 2, dtype=torch.int32)
+    topk_w = torch.zeros(16, 4)[:, :2]               # column slice
+    y_out = torch.zeros(16, 64)
+    ws = torch.zeros(256, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="not contiguous"):
+        B.smoe_combine(d, y_disp.t(), pair_row, topk_w.contiguous(), y_out, ws, stream=0)
+    with pytest.raises(ValueError, match="not contiguous"):
+        B.smoe_combine(d, y_disp.t().contiguous(), pair_row, topk_w, y_out, ws, stream=0)
+    assert B._ptr(y_out[3:7]) == y_out.data_ptr() + 3 * 64 * 4   # a row range stays dense
