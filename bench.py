@@ -321,7 +321,8 @@ class Workload:
             self.prefetch = dict(r=r, d_l=d_l, wgn=wgn.to(cfg.torch_dtype), gamma=gamma, beta=beta,
                                  pi=torch.empty(T, K, **i32), ti=torch.empty(T, K, **i32),
                                  hits=torch.zeros(1, dtype=torch.int64, device=dev))
-        torch.cuda.synchronize()
+        if dev.type == "cuda":
+            torch.cuda.synchronize()
 
     STAGES = ("route", "predict_shuffle", "lar", "dispatch", "expert_ffn", "combine", "prefetch")
 

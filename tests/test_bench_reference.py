@@ -1,0 +1,51 @@
+"""bench.py's reference arm (the CPU oracle on the host's cores) keeps the JSON-line
+contract and runs on rank 0 only. It needs no GPU, so it is checked here on the CPU
+with the smallest workload."""
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+ARGS = ["--impl", "reference", "--workload", "tiny_fp32", "--steps", "2", "--warmup", "3",
+        "--cpu-seconds", "1"]
+
+
+def setup_module():
+    # the workload's descriptor helpers live in the C library (host calls only)
+    from routing_token_shuffle_gb300 import build
+    build.build()
+
+
+def _run(env_extra):
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    env.update(env_extra)
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *ARGS], cwd=ROOT,
+                          env=env, capture_output=True, text=True, timeout=600)
+
+
+def test_reference_arm_prints_one_contract_line():
+    r = _run({})
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    out = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in out, key
+    assert out["impl"] == "reference"
+    assert out["steps"] == 2 and out["warmup"] == 3 and out["n_gpus"] == 1
+    assert out["unit"] == "tokens/s" and out["higher_is_better"] is True
+    assert out["value"] > 0
+    assert out["config"]["workload"].startswith("tiny_fp32: T=64")
+    cb = out["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == out["value"] and cb["cores"] >= 1
+    assert out["e2e"] == {"value": out["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                          "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    r = _run({"RANK": "1", "LOCAL_RANK": "1", "WORLD_SIZE": "2"})
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert not [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
