@@ -38,6 +38,16 @@ MUTATIONS = [
     ("topk_select: slot order within a group reversed",
      "idx[:, h * kh + j] = h * per + a",
      "idx[:, h * kh + (kh - 1 - j)] = h * per + a"),
+    ("topk_select: selection on float64 instead of float32 logits",
+     "    logits = np.asarray(logits, dtype=np.float32)\n    T, E = logits.shape\n    assert E % H",
+     "    logits = np.asarray(logits, dtype=np.float64)\n    T, E = logits.shape\n    assert E % H"),
+    ("gate_logits: not rounded to float32",
+     "return (x64 @ w64.T).astype(np.float32)",
+     "return (x64 @ w64.T)"),
+    ("selection_margin: maximum over groups instead of minimum",
+     "margin = np.minimum(margin, sub[:, kh - 1] - sub[:, kh])",
+     "margin = np.where(np.isinf(margin), sub[:, kh - 1] - sub[:, kh],"
+     " np.maximum(margin, sub[:, kh - 1] - sub[:, kh]))"),
     ("gate_weights: softmax over tokens instead of experts",
      "g = ex / ex.sum(axis=1, keepdims=True)",
      "g = ex / ex.sum(axis=0, keepdims=True)"),
@@ -58,6 +68,14 @@ MUTATIONS = [
     ("predict_partition: scores overwritten, not summed",
      "        score[:, emap[e]] = score[:, emap[e]] + rows[:, e]   # float32",
      "        score[:, emap[e]] = rows[:, e]   # float32"),
+    ("predict_partition: scores summed in float64",
+     "    score = np.zeros((len(ids), P), dtype=np.float32)\n    for e in range(conf.shape[1]):\n"
+     "        score[:, emap[e]] = score[:, emap[e]] + rows[:, e]   # float32",
+     "    score = np.zeros((len(ids), P), dtype=np.float64)\n    for e in range(conf.shape[1]):\n"
+     "        score[:, emap[e]] = score[:, emap[e]] + rows[:, e]   # float32"),
+    ("predict_partition: experts summed in descending order",
+     "    for e in range(conf.shape[1]):\n        score[:, emap[e]] = score[:, emap[e]] + rows[:, e]   # float32",
+     "    for e in reversed(range(conf.shape[1])):\n        score[:, emap[e]] = score[:, emap[e]] + rows[:, e]   # float32"),
     ("predict_partition: expert map ignored",
      "        score[:, emap[e]] = score[:, emap[e]] + rows[:, e]   # float32",
      "        score[:, e % P] = score[:, e % P] + rows[:, e]   # float32"),
@@ -102,6 +120,15 @@ MUTATIONS = [
     ("expert_dispatch: pairs in (k, s) order",
      "tok_of_q = np.repeat(perm, K)\n    k_of_q = np.tile(np.arange(K), T)",
      "tok_of_q = np.tile(perm, K)\n    k_of_q = np.repeat(np.arange(K), T)"),
+    ("expert_dispatch: unstable sort by expert",
+     'order = np.argsort(exp_of_q, kind="stable")',
+     'order = np.argsort(exp_of_q, kind="quicksort")'),
+    ("lar_counts: total counts a shared expert per token",
+     "return np.array([local, T * K, base_local, max_local], dtype=np.uint64)",
+     "return np.array([local, T * (K + 1), base_local, max_local], dtype=np.uint64)"),
+    ("foe_source: H >= G groups spread round-robin",
+     "return (h * G) // H",
+     "return h % G"),
     ("expert_dispatch: shuffle ignored",
      "perm = np.arange(T) if shuf_perm is None else np.asarray(shuf_perm, dtype=np.int64)",
      "perm = np.arange(T)"),
@@ -140,6 +167,15 @@ MUTATIONS = [
     ("layer_norm: eps dropped",
      "return (v - mu) / np.sqrt(var + eps)",
      "return (v - mu) / np.sqrt(var)"),
+    ("layer_norm: eps added outside the square root",
+     "return (v - mu) / np.sqrt(var + eps)",
+     "return (v - mu) / (np.sqrt(var) + eps)"),
+    ("prefetch_predict: residual dropped from the true next input",
+     "s = layer_norm(np.asarray(r, np.float64) + np.asarray(y, np.float64), gamma, beta, eps)",
+     "s = layer_norm(np.asarray(y, np.float64), gamma, beta, eps)"),
+    ("speculative_execution: deviation relative to the speculative output",
+     "dev = float(np.linalg.norm(y_spec - y_true) / max(np.linalg.norm(y_true), 1e-300))",
+     "dev = float(np.linalg.norm(y_spec - y_true) / max(np.linalg.norm(y_spec), 1e-300))"),
     ("layer_norm: unbiased variance",
      "var = ((v - mu) ** 2).mean(axis=-1, keepdims=True)",
      "var = ((v - mu) ** 2).sum(axis=-1, keepdims=True) / (v.shape[-1] - 1)"),

@@ -144,6 +144,24 @@ def test_gate_logits_exact_small_integers():
     assert O.gate_logits(x, wg).tolist() == exp
 
 
+def test_gate_logits_rounded_once_to_float32():
+    """Logits are float32 (one rounding of the exact dot product): 1 + 2^-30 is 1.0."""
+    x = np.array([[1.0, 2.0 ** -30]])
+    wg = np.array([[1.0, 1.0], [1.0, -1.0]])
+    out = O.gate_logits(x, wg)
+    assert out.dtype == np.float32
+    assert out.tolist() == [[1.0, 1.0]]
+
+
+def test_topk_compares_float32_logits():
+    """Selection compares float32 values: logits that differ only below float32 resolution
+    are a tie, which the lower index wins."""
+    logits = np.array([[1.0, 1.0 + 1e-12, 0.0, -1.0],
+                       [-1.0, 0.5 + 1e-13, 0.5, 0.25]])
+    assert O.topk_select(logits, 1).tolist() == [[0], [1]]
+    assert O.topk_select(logits, 2).tolist() == [[0, 1], [1, 2]]
+
+
 # ------------------------------------------------ predicted partition --------
 
 
@@ -161,6 +179,20 @@ def test_predict_exact_rationals():
               for p in range(P)]
         best = max(sc)
         assert pred[t] == sc.index(best)
+
+
+def test_predict_scores_are_float32_sums_in_ascending_expert_order():
+    """Partition scores add the C_p entries of the partition's experts one float32 add at a
+    time, in ascending expert order; equal scores go to the lower partition.
+    Row 0: partition 1 sums 1 + 2^-24, which rounds to 1.0 (half an ulp, to even), so it
+    ties partition 0's 1.0 and partition 0 wins (a float64 sum would pick 1).
+    Row 1: partition 1's entries 2^-24, 2^-24, 1 sum to 1 + 2^-23 in ascending order and
+    beat partition 0's 1.0 (in descending order they would round back to 1.0 and tie)."""
+    tiny = np.float32(2.0 ** -24)
+    conf = np.array([[1.0, 1.0, tiny, 0.0],
+                     [1.0, tiny, tiny, 1.0]], dtype=np.float32)
+    emap = np.array([0, 1, 1, 1], np.int32)
+    assert O.predict_partition(np.array([0, 1]), conf, emap, 2).tolist() == [0, 1]
 
 
 def test_predict_single_partition():
