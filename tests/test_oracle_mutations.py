@@ -167,6 +167,21 @@ MUTATIONS = [
     ("layer_norm: eps dropped",
      "return (v - mu) / np.sqrt(var + eps)",
      "return (v - mu) / np.sqrt(var)"),
+    ("layer_forward: dispatch ignores the shuffle",
+     "expert_off, pair_row, row_token = expert_dispatch(idx, E, shuf_perm)\n    y = moe_output",
+     "expert_off, pair_row, row_token = expert_dispatch(idx, E)\n    y = moe_output"),
+    ("layer_forward: renormalisation not passed on",
+     "    w = gate_weights(logits, idx, renorm)\n    E = np.asarray(w_gate).shape[0]",
+     "    w = gate_weights(logits, idx)\n    E = np.asarray(w_gate).shape[0]"),
+    ("coclustering_cost: imbalance from max - min",
+     "imbalance = (load.max() - mean) / mean if mean > 0 else 0.0",
+     "imbalance = (load.max() - load.min()) / mean if mean > 0 else 0.0"),
+    ("coclustering_cost: local activations counted as remote",
+     "if m[e] != tau[v])",
+     "if m[e] == tau[v])"),
+    ("markov_table: rows normalised by column sums",
+     "rows = counts.sum(axis=1, keepdims=True)",
+     "rows = counts.sum(axis=0, keepdims=True)"),
     ("layer_norm: eps added outside the square root",
      "return (v - mu) / np.sqrt(var + eps)",
      "return (v - mu) / (np.sqrt(var) + eps)"),
@@ -198,6 +213,9 @@ MUTATIONS = [
     ("profile_confidence: farthest id fills unseen rows",
      "nn = np.argmax(eu @ es.T, axis=1)",
      "nn = np.argmin(eu @ es.T, axis=1)"),
+    ("profile_confidence: nearest by dot product instead of cosine",
+     "            es = es / np.linalg.norm(es, axis=1, keepdims=True)\n",
+     "            es = es\n"),
     ("profile_confidence: fill 1/E instead of K/E",
      "conf = np.full((vocab, E), K / E, dtype=np.float64)",
      "conf = np.full((vocab, E), 1.0 / E, dtype=np.float64)"),

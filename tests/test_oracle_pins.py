@@ -501,6 +501,44 @@ def test_dispatched_path_equals_definition(S, H, K, E):
         np.testing.assert_allclose(out["y"][t], exp, rtol=1e-12, atol=1e-12)
 
 
+def test_layer_dispatch_follows_the_shuffle():
+    """Inside each expert's segment the layer's dispatch orders pairs by (shuffled slot of
+    the token, k), and every row maps back to its pair: checked against the layer's own
+    predicted partitions, which differ from token order here."""
+    x, ids, wg, w1, w3, w2, conf, emap = tiny_layer(seed=52, T=40, E=8, K=3, P=4)
+    out = O.layer_forward(x, ids, wg, w1, w3, w2, conf, emap, K=3, P=4)
+    perm, idx, pr, rt, eo = (out[k] for k in ("shuf_perm", "idx", "pair_row", "row_token",
+                                              "expert_off"))
+    assert not np.array_equal(perm, np.arange(40))
+    slot = np.empty(40, np.int64)
+    slot[perm] = np.arange(40)
+    for e in range(8):
+        keys = []
+        for r in range(eo[e], eo[e + 1]):
+            t = int(rt[r])
+            k = [kk for kk in range(3) if pr[t, kk] == r]
+            assert len(k) == 1 and idx[t, k[0]] == e
+            keys.append((int(slot[t]), k[0]))
+        assert keys == sorted(keys)
+
+
+def test_layer_renormalised_weights():
+    """With renorm the layer's K weights per token sum to 1 and are the plain weights
+    scaled by their sum; the output is the weighted sum with those weights."""
+    x, ids, wg, w1, w3, w2, conf, emap = tiny_layer(seed=53, T=30, E=8, K=2)
+    plain = O.layer_forward(x, ids, wg, w1, w3, w2, conf, emap, K=2, P=2)
+    ren = O.layer_forward(x, ids, wg, w1, w3, w2, conf, emap, K=2, P=2, renorm=True)
+    np.testing.assert_allclose(ren["w"].sum(axis=1), 1.0, rtol=1e-13)
+    np.testing.assert_allclose(ren["w"], plain["w"] / plain["w"].sum(axis=1, keepdims=True),
+                               rtol=1e-13)
+    y = np.zeros_like(ren["y"])
+    for t in range(30):
+        for k in range(2):
+            e = ren["idx"][t, k]
+            y[t] += ren["w"][t, k] * O.swiglu_ffn(x[t:t + 1], w1[e], w3[e], w2[e])[0]
+    np.testing.assert_allclose(ren["y"], y, rtol=1e-12, atol=1e-12)
+
+
 def test_lossless_invariant():
     """The shuffle and the prediction do not change the layer output (Speculative MoE
     summary: lossless), and permuting tokens permutes the output."""
@@ -570,6 +608,20 @@ def test_profile_confidence_counts_and_oov():
     np.testing.assert_allclose(conf[[0, 1, 3]].sum(axis=1), 2.0)      # K per seen row
     empty = O.profile_confidence(np.zeros(0, np.int32), np.zeros((0, 2), np.int32), 3, 4, 2)
     np.testing.assert_allclose(empty, 0.5)
+
+
+def test_profile_confidence_oov_is_cosine_not_dot_product():
+    """An unseen id takes the row of the seen id at the smallest angle, not the largest dot
+    product: id 4 = (0.3, 1) is at the same angle to ids 1 = (0, 1) and 3 = (0, 2), so the
+    lower id (1) wins, although id 3's dot product is twice id 1's."""
+    ids = np.array([0, 1, 3, 3], np.int32)
+    idx = np.array([[0, 1], [1, 2], [3, 0], [0, 3]], np.int32)
+    emb = np.array([[1.0, 0.0], [0.0, 1.0], [5.0, 5.0], [0.0, 2.0], [0.3, 1.0]])
+    conf = O.profile_confidence(ids, idx, 5, 4, 2, emb_rows=lambda v: emb[np.asarray(v)],
+                                rows_needed=np.array([4]))
+    np.testing.assert_array_equal(conf[4], conf[1])
+    assert not np.array_equal(conf[1], conf[3])
+    np.testing.assert_allclose(conf[2], 0.5)          # unseen and not needed: K/E
 
 
 # ------------------------------------------------- inter-layer predictor -----
