@@ -167,6 +167,18 @@ MUTATIONS = [
     ("layer_norm: eps dropped",
      "return (v - mu) / np.sqrt(var + eps)",
      "return (v - mu) / np.sqrt(var)"),
+    ("route: groups dropped",
+     "    idx = topk_select(logits, K, H)\n    return logits, idx, gate_weights(logits, idx, renorm)",
+     "    idx = topk_select(logits, K)\n    return logits, idx, gate_weights(logits, idx, renorm)"),
+    ("layer_forward: groups dropped",
+     "    idx = topk_select(logits, K, H)\n    w = gate_weights(logits, idx, renorm)\n    E =",
+     "    idx = topk_select(logits, K)\n    w = gate_weights(logits, idx, renorm)\n    E ="),
+    ("prefetch_predict: true routes without groups",
+     "true_idx = topk_select(logits_s, K, H)",
+     "true_idx = topk_select(logits_s, K)"),
+    ("predict_partition_inter: last largest entry of the A row",
+     "pred_inter = np.argmax(a_rows, axis=1)",
+     "pred_inter = P - 1 - np.argmax(a_rows[:, ::-1], axis=1)"),
     ("layer_forward: dispatch ignores the shuffle",
      "expert_off, pair_row, row_token = expert_dispatch(idx, E, shuf_perm)\n    y = moe_output",
      "expert_off, pair_row, row_token = expert_dispatch(idx, E)\n    y = moe_output"),

@@ -522,6 +522,31 @@ def test_layer_dispatch_follows_the_shuffle():
         assert keys == sorted(keys)
 
 
+def _group_picks_ok(logits, idx, K, H):
+    """Slots [h K/H, (h+1) K/H) hold group h's K/H best experts (brute force per group)."""
+    T, E = logits.shape
+    per, kh = E // H, K // H
+    for t in range(T):
+        for h in range(H):
+            got = [int(e) - h * per for e in idx[t, h * kh:(h + 1) * kh]]
+            if got != brute_topk(logits[t, h * per:(h + 1) * per].tolist(), kh):
+                return False
+    return True
+
+
+@pytest.mark.parametrize("H,K", [(2, 2), (4, 4), (2, 4)])
+def test_route_and_layer_pick_within_groups(H, K):
+    """The router and the layer both select per group: slot block h holds the K/H best
+    experts of group h, by brute force on the float32 logits."""
+    x, ids, wg, w1, w3, w2, conf, emap = tiny_layer(seed=60 + H + K, T=40, E=8, K=K, H=H)
+    logits, idx, _ = O.route(x, wg, K, H)
+    assert _group_picks_ok(logits, idx, K, H)
+    out = O.layer_forward(x, ids, wg, w1, w3, w2, conf, emap, K=K, H=H, P=2)
+    assert _group_picks_ok(out["logits"], out["idx"], K, H)
+    # the plain top-K differs from the grouped picks on this batch
+    assert not _group_picks_ok(logits, O.topk_select(logits, K), K, H)
+
+
 def test_layer_renormalised_weights():
     """With renorm the layer's K weights per token sum to 1 and are the plain weights
     scaled by their sum; the output is the weighted sum with those weights."""
@@ -684,6 +709,19 @@ def test_inter_never_confident_reduces_to_intra():
     prev = rng.integers(0, P, size=T)
     assert np.array_equal(O.predict_partition_inter(ids, conf, emap, P, K, prev, uni),
                           O.predict_partition(ids, conf, emap, P))
+
+
+def test_inter_prediction_ties_go_to_the_lower_partition():
+    """When table A is the more confident source and its row has two largest entries, the
+    inter-layer prediction is the lower partition. Intra confidence here: each C_p row is
+    spread evenly (score K/P per partition -> 1/P = 1/3 < 0.5)."""
+    V, E, K, P = 4, 6, 3, 3
+    conf = np.full((V, E), K / E, np.float32)
+    emap = (np.arange(E) % P).astype(np.int32)
+    a = np.array([[0.0, 0.5, 0.5], [0.5, 0.0, 0.5], [0.5, 0.5, 0.0]], np.float32)
+    prev = np.array([0, 1, 2, 0])
+    got = O.predict_partition_inter(np.arange(V), conf, emap, P, K, prev, a)
+    assert got.tolist() == [1, 0, 0, 1]
 
 
 def test_speculative_execution_pins():
