@@ -234,6 +234,15 @@ MUTATIONS = [
     ("coclustering_cost: theta on the wrong term",
      "return theta * imbalance + (1.0 - theta) * (remote / total",
      "return (1.0 - theta) * imbalance + theta * (remote / total"),
+    ("coclustering_bruteforce: balance constraint dropped",
+     "if any(m.count(p) != E // P for p in range(P)):",
+     "if False:"),
+    ("coclustering_bruteforce: the last of equal-cost optima kept",
+     "if c < best[0] - 1e-15:",
+     "if c <= best[0] + 1e-15:"),
+    ("coclustering_bruteforce: the last token never tried outside cluster 0",
+     "for tau in itertools.product(range(P), repeat=V):",
+     "for tau in itertools.product(*([range(P)] * (V - 1) + [range(1)])):"),
     ("rho_foe: max instead of min",
      "return min(H / G, 1.0)",
      "return max(H / G, 1.0)"),

@@ -772,3 +772,22 @@ def test_coclustering_cost_hand():
     assert abs(O.coclustering_cost(act, [0, 0, 1, 1], [0, 0], 2, 0.25) - 0.625) < 1e-15
     # expert map (0,1,0,1): token 0 loses expert 1 (1), token 1 loses expert 2 (2) -> 3/8
     assert abs(O.coclustering_cost(act, [0, 1, 0, 1], [0, 1], 2, 0.0) - 0.375) < 1e-15
+
+
+def test_coclustering_bruteforce_hand_enumerated():
+    """The exhaustive co-clustering search returns the first optimum of a hand-enumerated
+    instance (golden/coclustering_hand.json): the cost, the balanced expert map and the
+    token map. Each balanced map's best token map and cost, worked by hand, are checked
+    through the cost function too."""
+    g = load("coclustering_hand.json")
+    act = np.array(g["act"], float)
+    P, theta = g["P"], g["theta"]
+    for row in g["per_map_best"]:
+        c = O.coclustering_cost(act, row["expert_part"], row["token_part"], P, theta)
+        assert abs(c - row["cost"]) < 1e-12, row
+    cost, m, tau = O.coclustering_bruteforce(act, P, theta)
+    opt = g["optimum"]
+    assert abs(cost - opt["cost"]) < 1e-12
+    assert m.tolist() == opt["expert_part"]
+    assert tau.tolist() == opt["token_part"]
+    assert all(int(np.sum(m == p)) == act.shape[1] // P for p in range(P))
