@@ -385,6 +385,63 @@ def layer_forward_dispatched(x, idx, w, w1, w3, w2, shuf_perm, n_shared=0):
 
 
 # ----------------------------------------------------------------------------
+# Expert-parallel exchange between P simulated devices   [sMoE §1 EP; §3.1 SRS/SAG]
+# ----------------------------------------------------------------------------
+
+
+def ep_exchange(idx, expert_part, P, src_part=None):
+    """The expert-parallel all-to-all dispatch that P devices would run [sMoE §1: each
+    token is sent from its device to the devices of its K experts, and the results come
+    back the same way]. Token t sits on device src(t): src_part[t] (the s-TS predicted
+    partition, §3.1), or the contiguous split floor(t P / T) when src_part is None.
+    Pair (t, k) goes to device dst = map[idx[t, k]]; a pair with dst == src stays local.
+
+    Device q's receive buffer holds its pairs from source 0, then source 1, ...; inside
+    one (dst, src) segment the pairs keep the source's token order, then k (what an
+    all2allv delivers from send buffers laid out that way). All P receive buffers are
+    concatenated, device 0 first, so the pairs are sorted by the key (dst, src, t, k).
+
+    Returns send_counts [P, P] int32 (pairs from device p to device q), recv_off
+    [P*P + 1] int32 (segment (dst q, src p) is rows recv_off[q P + p] .. recv_off[q P +
+    p + 1]), pair_recv [T, K] int32 (row of pair (t, k)) and recv_token [T K] int32
+    (token of each row)."""
+    idx = np.asarray(idx, dtype=np.int64)
+    emap = np.asarray(expert_part, dtype=np.int64)
+    T, K = idx.shape
+    t = np.arange(T)
+    src = (t * P) // max(T, 1) if src_part is None else np.asarray(src_part, dtype=np.int64)
+    tok = np.repeat(t, K)                      # pairs enumerated in (t, k) order
+    kk = np.tile(np.arange(K), T)
+    dst = emap[idx[tok, kk]]
+    key = dst * P + src[tok]
+    order = np.argsort(key, kind="stable")     # receive row r -> pair
+    counts = np.bincount(key, minlength=P * P)
+    recv_off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    send_counts = counts.reshape(P, P).T.astype(np.int32)   # [src, dst]
+    pair_recv = np.empty((T, K), dtype=np.int32)
+    pair_recv[tok[order], kk[order]] = np.arange(T * K, dtype=np.int32)
+    return send_counts, recv_off, pair_recv, tok[order].astype(np.int32)
+
+
+def shuffled_reduce_scatter(x_parts, shuf_perm):
+    """SRS [sMoE §3.1]: the R tensor-parallel partial sums of the activations are added
+    and each token lands in the slot the speculative shuffle gave it, so partition p
+    receives the reduced rows of the tokens predicted for it (slots part_off[p] ..).
+    x_parts [R, T, d]; returns float64 [T, d] in slot order."""
+    x = np.asarray(x_parts, dtype=np.float64)
+    return x.sum(axis=0)[np.asarray(shuf_perm, dtype=np.int64)]
+
+
+def shuffled_allgather(y_shuf, shuf_perm):
+    """SAG [sMoE §3.1]: rows held in slot order are returned to token order,
+    y[shuf_perm[s]] = y_shuf[s]."""
+    y_shuf = np.asarray(y_shuf)
+    y = np.empty_like(y_shuf)
+    y[np.asarray(shuf_perm, dtype=np.int64)] = y_shuf
+    return y
+
+
+# ----------------------------------------------------------------------------
 # a10: next-layer prefetch predictor                                 [SpecE §2.A]
 # ----------------------------------------------------------------------------
 

@@ -243,6 +243,26 @@ MUTATIONS = [
     ("coclustering_bruteforce: the last token never tried outside cluster 0",
      "for tau in itertools.product(range(P), repeat=V):",
      "for tau in itertools.product(*([range(P)] * (V - 1) + [range(1)])):"),
+    ("ep_exchange: receive layout source-major",
+     "key = dst * P + src[tok]",
+     "key = src[tok] * P + dst"),
+    ("ep_exchange: send counts not transposed to [src, dst]",
+     "send_counts = counts.reshape(P, P).T.astype(np.int32)",
+     "send_counts = counts.reshape(P, P).astype(np.int32)"),
+    ("ep_exchange: contiguous split off by one",
+     "src = (t * P) // max(T, 1) if src_part is None",
+     "src = (t * P) // (T + 1) if src_part is None"),
+    ("ep_exchange: pairs enumerated k-major",
+     "    tok = np.repeat(t, K)                      # pairs enumerated in (t, k) order\n"
+     "    kk = np.tile(np.arange(K), T)",
+     "    tok = np.tile(t, K)                      # pairs enumerated in (t, k) order\n"
+     "    kk = np.repeat(np.arange(K), T)"),
+    ("shuffled_reduce_scatter: summed over tokens instead of ranks",
+     "return x.sum(axis=0)[np.asarray(shuf_perm, dtype=np.int64)]",
+     "return x.sum(axis=1, keepdims=True).repeat(x.shape[1], 1)[0][np.asarray(shuf_perm, dtype=np.int64)]"),
+    ("shuffled_allgather: gathers instead of scattering",
+     "y[np.asarray(shuf_perm, dtype=np.int64)] = y_shuf",
+     "y[:] = y_shuf[np.asarray(shuf_perm, dtype=np.int64)]"),
     ("rho_foe: max instead of min",
      "return min(H / G, 1.0)",
      "return max(H / G, 1.0)"),

@@ -791,3 +791,69 @@ def test_coclustering_bruteforce_hand_enumerated():
     assert m.tolist() == opt["expert_part"]
     assert tau.tolist() == opt["token_part"]
     assert all(int(np.sum(m == p)) == act.shape[1] // P for p in range(P))
+
+
+# ------------------------------------------ expert-parallel exchange (EP) ------
+
+
+@pytest.mark.parametrize("case", ["sts", "contiguous"])
+def test_ep_exchange_fig2_golden(case):
+    g = load("ep_exchange_fig2_hand.json")
+    src = g["pred"] if case == "sts" else None
+    sc, ro, pr, rt = O.ep_exchange(np.array(g["routes"]), g["expert_part"], g["P"], src)
+    want = g[case]
+    assert sc.tolist() == want["send_counts"]
+    assert ro.tolist() == want["recv_off"]
+    assert rt.tolist() == want["recv_token"]
+    assert pr.tolist() == want["pair_recv"]
+
+
+@pytest.mark.parametrize("T,E,K,P,shuffled", [(1, 4, 2, 2, True), (37, 8, 2, 2, True),
+                                               (64, 16, 4, 4, False), (200, 160, 6, 8, True),
+                                               (50, 12, 3, 3, False)])
+def test_ep_exchange_invariants(T, E, K, P, shuffled):
+    """Counts by a direct double loop; the receive layout is a bijection whose segment
+    offsets are the scan of those counts read destination-major; the key (dst, src) never
+    decreases along it and (t, k) increases inside a segment; the local pairs are the
+    alpha count of the same sources."""
+    rng = np.random.default_rng(T * 7 + E)
+    idx = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+    emap = rng.integers(0, P, E).astype(np.int32)
+    src = rng.integers(0, P, T).astype(np.int32) if shuffled else None
+    sc, ro, pr, rt = O.ep_exchange(idx, emap, P, src)
+    srcv = src if shuffled else np.array([t * P // T for t in range(T)])
+    direct = np.zeros((P, P), int)
+    for t in range(T):
+        for k in range(K):
+            direct[srcv[t], emap[idx[t, k]]] += 1
+    assert sc.tolist() == direct.tolist()
+    run = [0]
+    for q in range(P):
+        for p in range(P):
+            run.append(run[-1] + direct[p, q])
+    assert ro.tolist() == run
+    assert sorted(pr.ravel().tolist()) == list(range(T * K))
+    keys = []
+    for r in range(T * K):
+        t, k = divmod(int(np.nonzero(pr.ravel() == r)[0][0]), K)
+        assert rt[r] == t
+        keys.append((emap[idx[t, k]], srcv[t], t, k))
+    assert keys == sorted(keys)
+    lar = O.lar_counts(idx, emap, P, src_part=srcv)
+    assert int(np.trace(sc)) == int(lar[0])
+    assert int(sc.sum()) == T * K
+
+
+def test_srs_sag_golden_and_round_trip():
+    g = load("ep_exchange_fig2_hand.json")["srs"]
+    red = O.shuffled_reduce_scatter(np.array(g["x_parts"]), g["shuf_perm"])
+    assert red.tolist() == g["reduced_in_slot_order"]
+    back = O.shuffled_allgather(red, g["shuf_perm"])
+    assert back.ravel().tolist() == [11.0, 22.0, 33.0]
+    rng = np.random.default_rng(3)
+    xp = rng.standard_normal((3, 40, 5))
+    perm = rng.permutation(40)
+    # one partial is the plain shuffle gather; the round trip restores token order
+    assert np.array_equal(O.shuffled_reduce_scatter(xp[:1], perm), xp[0][perm])
+    np.testing.assert_allclose(O.shuffled_allgather(O.shuffled_reduce_scatter(xp, perm), perm),
+                               xp[0] + xp[1] + xp[2], rtol=0, atol=1e-15)
