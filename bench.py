@@ -30,11 +30,20 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-DEFAULT_WORKLOAD = "mixtral"
+DEFAULT_WORKLOAD = "dsv2_prefill"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
 # ----------------------------------------------------------------- helpers
+
+METRIC = ("MoE-layer tokens/s (gate+top-K, s-TS predict+shuffle, LAR, dispatch, grouped SwiGLU "
+          "FFN, combine) on GB300")
+
+
+def workload_label(cfg) -> str:
+    return (f"{cfg.name}: T={cfg.T}, d={cfg.d}, E={cfg.E}, K={cfg.K}, H={cfg.H}, F={cfg.F}, "
+            f"shared={cfg.n_shared}, P={cfg.P}, vocab={cfg.vocab}")
+
 
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
@@ -208,8 +217,8 @@ class ClockSampler:
 class Workload:
     """Device-resident inputs of one workload and the per-stage C-ABI calls of a step."""
 
-    def __init__(self, name: str, device, rank: int = 0, prepare_with_oracle: bool = False,
-                 tokens: int | None = None, seed: int = 0):
+    def __init__(self, name: str, device, rank: int = 0, tokens: int | None = None,
+                 seed: int = 0):
         import numpy as np
         import torch
 
@@ -232,26 +241,21 @@ class Workload:
         self.w_gate, self.w1, self.w3, self.w2 = synth.layer_weights_lowp(cfg, dev)
         self.emap = synth.placement_identity(cfg)
         self.desc = smoe.desc_from_config(cfg)
-        self.ws = None if prepare_with_oracle else smoe.workspace(self.desc, dev)
+        self.ws = smoe.workspace(self.desc, dev)
         # offline C_p: route a seeded profiling batch with the library, count on the host
         n_prof = cfg.profile_tokens
         pids, px = synth.token_batch(cfg, self.emb, "profile", n_prof, dev)
         px = px.to(cfg.torch_dtype)
         chunk = min(n_prof, 8192)
         pdesc = smoe.desc_from_config(cfg, T=chunk)
-        if prepare_with_oracle:
-            import oracle as O
-            _, self.profile_idx, _ = O.route(px.float().cpu().numpy(),
-                                             self.w_gate.float().cpu().numpy(), cfg.K, cfg.H)
-        else:
-            pws = smoe.workspace(pdesc, dev)
-            pidx = torch.empty(n_prof, cfg.K, dtype=torch.int32, device=dev)
-            pw = torch.empty(chunk, cfg.K, device=dev)
-            for lo in range(0, n_prof, chunk):
-                smoe.smoe_route(pdesc, px[lo:lo + chunk], self.w_gate, pidx[lo:lo + chunk], pw,
-                                ws=pws)
-            self.profile_idx = pidx.cpu().numpy()
-            del pw, pws
+        pws = smoe.workspace(pdesc, dev)
+        pidx = torch.empty(n_prof, cfg.K, dtype=torch.int32, device=dev)
+        pw = torch.empty(chunk, cfg.K, device=dev)
+        for lo in range(0, n_prof, chunk):
+            smoe.smoe_route(pdesc, px[lo:lo + chunk], self.w_gate, pidx[lo:lo + chunk], pw,
+                            ws=pws)
+        self.profile_idx = pidx.cpu().numpy()
+        del pw, pws
         del px
         self.profile_ids = pids
         self.conf = profiling.confidence_table(
@@ -284,29 +288,27 @@ class Workload:
                                           self.emap_d)
         # inter-layer predictor inputs: a stand-in previous layer routes the profile batch and
         # the measured batch; table A counts cluster transitions on the profile batch
-        self.inter = None
-        if not prepare_with_oracle:
-            wprev = synth.previous_layer_gate(cfg, dev)
-            _, px2 = synth.token_batch(cfg, self.emb, "profile", n_prof, dev)
-            px2 = px2.to(cfg.torch_dtype)
-            pprev = torch.empty(n_prof, cfg.K, dtype=torch.int32, device=dev)
-            pws2 = smoe.workspace(pdesc, dev)
-            pw2 = torch.empty(chunk, cfg.K, device=dev)
-            for lo in range(0, n_prof, chunk):
-                smoe.smoe_route(pdesc, px2[lo:lo + chunk], wprev, pprev[lo:lo + chunk], pw2,
-                                ws=pws2)
-            table = profiling.transition_table(
-                profiling.cluster_of(pprev.cpu().numpy(), self.emap, cfg.P),
-                profiling.cluster_of(self.profile_idx, self.emap, cfg.P), cfg.P)
-            del px2, pws2, pw2, pprev
-            bidx = torch.empty(cfg.T, cfg.K, dtype=torch.int32, device=dev)
-            bw = torch.empty(cfg.T, cfg.K, device=dev)
-            smoe.smoe_route(self.desc, self.x, wprev, bidx, bw, ws=self.ws)
-            prev_cluster = torch.empty(cfg.T, dtype=torch.int32, device=dev)
-            smoe.smoe_token_cluster(self.desc, bidx, self.emap_d, prev_cluster, self.ws)
-            self.inter = dict(prev=prev_cluster, table=torch.as_tensor(table, device=dev))
+        wprev = synth.previous_layer_gate(cfg, dev)
+        _, px2 = synth.token_batch(cfg, self.emb, "profile", n_prof, dev)
+        px2 = px2.to(cfg.torch_dtype)
+        pprev = torch.empty(n_prof, cfg.K, dtype=torch.int32, device=dev)
+        pws2 = smoe.workspace(pdesc, dev)
+        pw2 = torch.empty(chunk, cfg.K, device=dev)
+        for lo in range(0, n_prof, chunk):
+            smoe.smoe_route(pdesc, px2[lo:lo + chunk], wprev, pprev[lo:lo + chunk], pw2,
+                            ws=pws2)
+        table = profiling.transition_table(
+            profiling.cluster_of(pprev.cpu().numpy(), self.emap, cfg.P),
+            profiling.cluster_of(self.profile_idx, self.emap, cfg.P), cfg.P)
+        del px2, pws2, pw2, pprev
+        bidx = torch.empty(cfg.T, cfg.K, dtype=torch.int32, device=dev)
+        bw = torch.empty(cfg.T, cfg.K, device=dev)
+        smoe.smoe_route(self.desc, self.x, wprev, bidx, bw, ws=self.ws)
+        prev_cluster = torch.empty(cfg.T, dtype=torch.int32, device=dev)
+        smoe.smoe_token_cluster(self.desc, bidx, self.emap_d, prev_cluster, self.ws)
+        self.inter = dict(prev=prev_cluster, table=torch.as_tensor(table, device=dev))
         self.prefetch = None
-        if cfg.prefetch and not prepare_with_oracle:
+        if cfg.prefetch:
             r, wgn, gamma, beta = synth.predictor_inputs(cfg, dev)
             # default vector d_l: mean layer output over a separate 1024-token batch
             _, xp = synth.profile_batch_for_default_vector(cfg, self.emb, dev)
@@ -452,25 +454,32 @@ def placement_report(wl):
 
 # ----------------------------------------------------------------- CPU oracle
 
-def cpu_oracle_rate(wl, target_s: float, max_tokens: int | None = None):
+class HostLayer:
+    """One workload's inputs as host float32 / int32 arrays, the form the CPU oracle takes."""
+
+    def __init__(self, cfg, x, ids, w_gate, w1, w3, w2, conf, emap):
+        self.cfg, self.x, self.ids, self.w_gate = cfg, x, ids, w_gate
+        self.w1, self.w3, self.w2, self.conf, self.emap = w1, w3, w2, conf, emap
+
+
+def host_layer_from_workload(wl) -> HostLayer:
+    """The native arm's device-resident inputs copied to the host (for the CPU baseline)."""
+    f = (lambda t: t.float().cpu().numpy())
+    return HostLayer(wl.cfg, f(wl.x), wl.ids, f(wl.w_gate), f(wl.w1), f(wl.w3), f(wl.w2),
+                     wl.conf, wl.emap)
+
+
+def cpu_oracle_rate(h: HostLayer, target_s: float, max_tokens: int | None = None):
     """Tokens/s of the CPU oracle on the first n tokens of the workload's batch, n sized
     so one timed pass takes about target_s seconds. Returns (rate, n, seconds, cores)."""
-    import numpy as np
-
     import oracle as O
-    cfg = wl.cfg
-    x = wl.x.float().cpu().numpy()
-    wg = wl.w_gate.float().cpu().numpy()
-    w1 = wl.w1.float().cpu().numpy()
-    w3 = wl.w3.float().cpu().numpy()
-    w2 = wl.w2.float().cpu().numpy()
-    ids, conf, emap = wl.ids, wl.conf, wl.emap
+    cfg = h.cfg
     cap = cfg.T if max_tokens is None else min(cfg.T, max_tokens)
 
     def run(n):
         t0 = time.perf_counter()
-        O.layer_forward(x[:n], ids[:n], wg, w1, w3, w2, conf, emap, K=cfg.K, H=cfg.H, P=cfg.P,
-                        n_shared=cfg.n_shared)
+        O.layer_forward(h.x[:n], h.ids[:n], h.w_gate, h.w1, h.w3, h.w2, h.conf, h.emap, K=cfg.K,
+                        H=cfg.H, P=cfg.P, n_shared=cfg.n_shared)
         return time.perf_counter() - t0
 
     n = min(cap, 16)
@@ -480,6 +489,35 @@ def cpu_oracle_rate(wl, target_s: float, max_tokens: int | None = None):
         t = run(n)
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     return n / t, n, t, cores
+
+
+def reference_inputs(name: str, tokens: int | None = None, seed: int = 0) -> HostLayer:
+    """The workload built on the host alone, for the reference arm: the seeded generator on
+    the CPU (same shapes and distributions; torch's CPU generator draws other values than
+    its CUDA one) and C_p profiled from the oracle's own routes. Neither the CUDA library
+    nor a GPU is touched."""
+    import dataclasses
+
+    import numpy as np
+
+    import oracle as O
+    from routing_token_shuffle_gb300 import synth
+    cfg = synth.CONFIGS[name]
+    if tokens is not None:
+        cfg = dataclasses.replace(cfg, T=tokens)
+    emb = synth.Embedding(cfg, "cpu")
+    ids, x = synth.token_batch(cfg, emb, "ids", cfg.T, "cpu", salt=1000 * seed)
+    w_gate, w1, w3, w2 = synth.layer_weights(cfg, "cpu")
+    wg = w_gate.numpy()
+    pids, px = synth.token_batch(cfg, emb, "profile", cfg.profile_tokens, "cpu")
+    pidx = np.empty((len(pids), cfg.K), np.int32)
+    for lo in range(0, len(pids), 8192):
+        _, pidx[lo:lo + 8192], _ = O.route(px[lo:lo + 8192].numpy(), wg, cfg.K, cfg.H)
+    del px
+    conf = O.profile_confidence(pids, pidx, cfg.vocab, cfg.E, cfg.K,
+                                emb_rows=lambda v: emb.rows(v).numpy(), rows_needed=ids)
+    return HostLayer(cfg, x.numpy(), ids, wg, w1.numpy(), w3.numpy(), w2.numpy(), conf,
+                     synth.placement_identity(cfg))
 
 
 # ----------------------------------------------------------------- arms
@@ -512,7 +550,7 @@ def run_native(args):
 
     nst = len(Workload.STAGES)
     start = torch.cuda.Event(enable_timing=True)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst)] for _ in range(args.steps)]
+    stop = torch.cuda.Event(enable_timing=True)
     uuid = None
     try:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
@@ -522,66 +560,92 @@ def run_native(args):
     barrier(active)
     torch.cuda.synchronize()
     sampler.start()
+    t_pre = time.time()
     t_s = time.perf_counter()
     while time.perf_counter() - t_s < 0.4:   # keep the GPU busy while nvidia-smi starts
         wl.step()
         torch.cuda.synchronize()
     barrier(active)
+    # the timed region: K steps back to back on one stream, one event on each side
     launches0 = smoe.kernel_launches()
     t_wall0 = time.time()
     wall0 = time.perf_counter()
     start.record()
     for i in range(args.steps):
-        wl.step(evs[i])
+        wl.step()
+    stop.record()
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     launches = smoe.kernel_launches() - launches0
     t_wall1 = time.time()
     barrier(active)
-    clocks = sampler.stop(window=(t_wall0, t_wall1))
-    total_ms = start.elapsed_time(evs[-1][-1])
+    total_ms = start.elapsed_time(stop)
+    total_ms_max = max_over_ranks(total_ms, active, device=dev)
+    ms_per_step = total_ms_max / args.steps
+    value = whole_job_rate(cfg.T * args.steps, world, total_ms_max / 1e3)
+
+    # per-stage breakdown: another K steps with an event after every stage (not part of
+    # the value above; the events cost a little, reported as stage_pass_ms_per_step)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst)] for _ in range(args.steps)]
+    start2 = torch.cuda.Event(enable_timing=True)
+    start2.record()
+    for i in range(args.steps):
+        wl.step(evs[i])
+    torch.cuda.synchronize()
+    t_wall2 = time.time()
+    # clocks: samples taken while the layer ran, from the untimed pre-roll through the
+    # timed region and the stage pass (all the same back-to-back steps)
+    clocks = sampler.stop(window=(t_pre, t_wall2))
+    if clocks is not None:
+        clocks["window_s"] = round(t_wall2 - t_pre, 3)
+        clocks["timed_region_s"] = round(t_wall1 - t_wall0, 3)
     stage_ms = {s: 0.0 for s in Workload.STAGES}
     for i in range(args.steps):
-        prev = start if i == 0 else evs[i - 1][-1]
+        prev = start2 if i == 0 else evs[i - 1][-1]
         for j, sname in enumerate(Workload.STAGES):
             stage_ms[sname] += prev.elapsed_time(evs[i][j])
             prev = evs[i][j]
     stage_ms = {k: v / args.steps for k, v in stage_ms.items()}
-    total_ms_max = max_over_ranks(total_ms, active, device=dev)
-    ms_per_step = total_ms_max / args.steps
-    value = whole_job_rate(cfg.T * args.steps, world, total_ms_max / 1e3)
+    stage_pass_ms = start2.elapsed_time(evs[-1][-1]) / args.steps
     smoe.smoe_get_status(wl.ws)
 
     # end to end through the host-buffer entry point (H2D of x and ids, the layer, D2H of
-    # y every step), pipelined the way a serving loop would: two streams and two
-    # workspaces in turn, so one step's copies overlap the other's kernels
+    # y every step). Two schedules: serial (one stream, each step's copies and kernels in
+    # turn) and pipelined the way a serving loop runs (two streams and two workspaces in
+    # turn, so one step's copies overlap the other step's kernels). The pipelined one is
+    # the reported value.
     xh = [wl.x.cpu().pin_memory() for _ in range(2)]
     ih = [torch.as_tensor(wl.ids).pin_memory() for _ in range(2)]
     yh = [torch.empty_like(xh[0]).pin_memory() for _ in range(2)]
     streams = [torch.cuda.current_stream(), torch.cuda.Stream()]
     wss = [wl.ws, smoe.workspace(wl.desc, dev)]
 
-    def e2e_step(i):
-        j = i & 1
+    def e2e_step(i, nstreams):
+        j = i % nstreams
         smoe.smoe_layer_forward_host(wl.desc, wl.weights, xh[j], ih[j], yh[j], wss[j],
                                      stream=streams[j])
 
-    for i in range(4):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    barrier(active)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(streams[0])
-    streams[1].wait_event(e0)
-    for i in range(args.steps):
-        e2e_step(i)
-    streams[0].wait_stream(streams[1])
-    e1.record(streams[0])
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), active, device=dev)
+    def e2e_run(nstreams):
+        for i in range(4):
+            e2e_step(i, nstreams)
+        torch.cuda.synchronize()
+        barrier(active)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(streams[0])
+        streams[1].wait_event(e0)
+        for i in range(args.steps):
+            e2e_step(i, nstreams)
+        streams[0].wait_stream(streams[1])
+        e1.record(streams[0])
+        torch.cuda.synchronize()
+        return max_over_ranks(e0.elapsed_time(e1), active, device=dev)
+
+    e2e_serial_ms = e2e_run(1)
+    e2e_ms = e2e_run(2)
     del wss
     e2e_value = whole_job_rate(cfg.T * args.steps, world, e2e_ms / 1e3)
+    e2e_serial_value = whole_job_rate(cfg.T * args.steps, world, e2e_serial_ms / 1e3)
     h2d = xh[0].numel() * xh[0].element_size() + ih[0].numel() * ih[0].element_size()
     d2h = yh[0].numel() * yh[0].element_size()
 
@@ -589,7 +653,11 @@ def run_native(args):
     # from its arithmetic intensity against the measured ridge point (decode-sized
     # batches touch every expert's weights for a few rows: HBM-bound).
     ffn_ms = stage_ms["expert_ffn"]
-    peak_tf = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    # the burst peak for a timed region under a second, the sustained (power-capped) one
+    # for a region of seconds
+    long_region = total_ms / 1e3 >= 1.0
+    peak_key = "bf16_tflops_sustained" if long_region else "bf16_tflops"
+    peak_tf = peaks.get(peak_key, FALLBACK_PEAKS[peak_key])
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     eo = wl.expert_off.cpu().numpy()
     touched = int((eo[1:] > eo[:-1]).sum())
@@ -610,7 +678,8 @@ def run_native(args):
         roofline = {"bound": "tensor", "achieved": round(achieved_tf, 2), "peak": peak_tf,
                     "unit": "TFLOP/s", "frac": round(achieved_tf / peak_tf, 4),
                     "traffic": traffic, "kernel": kernel_name,
-                    "peak_kind": f"{peaks_kind} bf16 sustained"}
+                    "peak_kind": f"{peaks_kind} bf16 {'sustained' if long_region else 'burst'}"
+                                 f" (timed region {total_ms / 1e3:.3f} s)"}
     else:
         achieved_gbs = fbytes / (ffn_ms / 1e3) / 1e9
         roofline = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm,
@@ -631,7 +700,7 @@ def run_native(args):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        rate, n, secs, cores = cpu_oracle_rate(wl, args.cpu_seconds)
+        rate, n, secs, cores = cpu_oracle_rate(host_layer_from_workload(wl), args.cpu_seconds)
         cpu = {"value": round(rate, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"first {n} of the {cfg.T} tokens of this workload's batch, the whole "
                          f"layer in float64 numpy ({secs:.1f} s)"}
@@ -656,21 +725,19 @@ def run_native(args):
         inter_info = {"alpha_sTS_inter": float(li[0] / li[1]),
                       "predict_shuffle_inter_ms": round(ev[0].elapsed_time(ev[1]) / 10, 4)}
     result = {
-        "metric": "MoE-layer tokens/s (gate+top-K, s-TS predict+shuffle, LAR, dispatch, grouped "
-                  "SwiGLU FFN, combine) on GB300",
+        "metric": METRIC,
         "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype,
         "data": "synthetic (seeded; random-init weights of the workload's shape)",
-        "config": {"workload": f"{cfg.name}: T={cfg.T}, d={cfg.d}, E={cfg.E}, K={cfg.K}, "
-                               f"H={cfg.H}, F={cfg.F}, shared={cfg.n_shared}, P={cfg.P}, "
-                               f"vocab={cfg.vocab}",
+        "config": {"workload": workload_label(cfg),
                    "global_batch": cfg.T * world, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (expert weights "
                          f"{3 * (cfg.E + cfg.n_shared) * cfg.F * cfg.d * cfg.elem_bytes / 1e9:.2f}"
                          " GB streamed every step)"},
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "schedule": "two streams and two workspaces in turn",
+                "serial_value": round(e2e_serial_value, 1)},
         "gpu_launches": int(launches),
         "roofline": roofline,
         "cpu_baseline": cpu,
@@ -679,6 +746,7 @@ def run_native(args):
         "alpha": {"sTS": float(lar[0] / lar[1]), "base": float(lar[2] / lar[1]),
                   "max": float(lar[3] / lar[1])},
         "wall_s_timed": round(wall, 3),
+        "stage_pass_ms_per_step": round(stage_pass_ms, 4),
     }
     if inter_info is not None:
         result["alpha"]["sTS_with_table_A"] = inter_info["alpha_sTS_inter"]
@@ -705,27 +773,24 @@ def run_native(args):
 
 
 def run_reference(args):
-    """The CPU oracle as it stands, on this host's cores, same workload and metric."""
+    """The CPU oracle as it stands, on this host's cores, same workload and metric. A pure
+    host process: inputs come from the seeded generator on the CPU, C_p from the oracle's
+    own routes; the CUDA library is never loaded and no CUDA context is created."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    import torch
-    dev = "cuda" if torch.cuda.is_available() else "cpu"
-    wl = Workload(args.workload, dev, prepare_with_oracle=True, tokens=args.tokens,
-                  seed=args.seed)
-    per_step = max(1.0, min(args.cpu_seconds, 150.0 / max(args.steps + args.warmup, 1)))
-    rate, n, secs, cores = cpu_oracle_rate(wl, per_step)
+    h = reference_inputs(args.workload, tokens=args.tokens, seed=args.seed)
+    cfg = h.cfg
+    per_step = max(1.0, min(args.cpu_seconds, 100.0 / max(args.steps + args.warmup, 1)))
+    rate, n, secs, cores = cpu_oracle_rate(h, per_step)
     import oracle as O
-    cfg = wl.cfg
-    x = wl.x.float().cpu().numpy()[:n]
-    wg = wl.w_gate.float().cpu().numpy()
-    w1, w3, w2 = (t.float().cpu().numpy() for t in (wl.w1, wl.w3, wl.w2))
+    x, ids = h.x[:n], h.ids[:n]
     for _ in range(args.warmup):
-        O.layer_forward(x, wl.ids[:n], wg, w1, w3, w2, wl.conf, wl.emap, K=cfg.K, H=cfg.H,
+        O.layer_forward(x, ids, h.w_gate, h.w1, h.w3, h.w2, h.conf, h.emap, K=cfg.K, H=cfg.H,
                         P=cfg.P, n_shared=cfg.n_shared)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        O.layer_forward(x, wl.ids[:n], wg, w1, w3, w2, wl.conf, wl.emap, K=cfg.K, H=cfg.H,
+        O.layer_forward(x, ids, h.w_gate, h.w1, h.w3, h.w2, h.conf, h.emap, K=cfg.K, H=cfg.H,
                         P=cfg.P, n_shared=cfg.n_shared)
     secs = time.perf_counter() - t0
     value = n * args.steps / secs
@@ -733,15 +798,12 @@ def run_reference(args):
               f"numpy")
     print(json.dumps({
         "impl": "reference",
-        "metric": "MoE-layer tokens/s (gate+top-K, s-TS predict+shuffle, LAR, dispatch, grouped "
-                  "SwiGLU FFN, combine) on GB300",
+        "metric": METRIC,
         "value": round(value, 3), "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded)",
-        "config": {"workload": f"{cfg.name}: T={cfg.T}, d={cfg.d}, E={cfg.E}, K={cfg.K}, "
-                               f"H={cfg.H}, F={cfg.F}, shared={cfg.n_shared}, P={cfg.P}",
-                   "global_batch": n},
+        "data": "synthetic (seeded, drawn on the host)",
+        "config": {"workload": workload_label(cfg), "global_batch": n},
         "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,

@@ -10,6 +10,8 @@
  *   grouped SwiGLU expert FFN                       -> smoe_expert_ffn
  *   dispatch's row copy + expert FFN in one call    -> smoe_expert_ffn_gather
  *   weighted combine back into token order          -> smoe_combine
+ *   EP all-to-all plan between simulated devices    -> smoe_ep_exchange
+ *   shuffled reduce-scatter / all-gather (SRS, SAG) -> smoe_srs, smoe_sag
  *   all of the above in one call                    -> smoe_layer_forward
  *   next-layer route predictor q = LN(d + r)        -> smoe_prefetch_predict
  *
@@ -151,17 +153,18 @@ SMOE_API int smoe_predict_shuffle_inter(const smoe_desc* desc, const int32_t* to
                                         size_t ws_bytes, void* stream);
 
 /* Workspace-free variant of smoe_predict_shuffle, for callers that cannot allocate
- * device memory: code running while a CUDA graph is being captured (where allocation
- * calls are not allowed), runtimes that forbid allocation after start-up, or hosts
- * whose device memory pool belongs to another framework. The pages have no
- * counterpart; it computes exactly what smoe_predict_shuffle computes, with the same
- * arguments minus the workspace.
+ * device memory: runtimes that reserve all their device memory at start-up and
+ * forbid allocation afterwards, or hosts whose device memory pool belongs to another
+ * framework that the library may not draw from. The pages have no counterpart; it
+ * computes exactly what smoe_predict_shuffle computes, with the same arguments minus
+ * the workspace.
  *   - Its histogram scratch is a 1 MB array inside the library that every GPU which
  *     loads the library holds until the process exits; T is limited to 1048576 tokens
  *     (4096 tiles of 256), larger T returns SMOE_ERR_SHAPE.
  *   - It allocates nothing and calls no allocating routine.
- *   - The first call on a device looks up that array's device address (with the
- *     device current); make that first call before any stream capture begins.
+ *   - The first call in a CUDA context of a device (the device's primary context, and
+ *     again after that context has been reset) looks up that array's device address
+ *     with the device current; make that first call before any stream capture begins.
  *   - All calls share the one array: calls that overlap on the GPU (different
  *     streams, or different host threads) race and must be serialised by the caller.
  *     Each call clears the histogram part of the array before using it and rewrites
@@ -243,6 +246,57 @@ SMOE_API int smoe_expert_ffn_gather(const smoe_desc* desc, const void* x_src,
 /* 1 when smoe_expert_ffn_gather copies the rows inside the up GEMM for this layer shape,
  * 0 when it copies them before the FFN (or the descriptor is invalid). Host only. */
 SMOE_API int smoe_expert_ffn_gather_fused(const smoe_desc* desc);
+
+/* Expert-parallel exchange between P simulated devices ("Speculative MoE" §1: under
+ * expert parallelism each token is sent from its device to the devices of its K
+ * experts, and the results are sent back). On one GPU nothing crosses a link: this
+ * builds the all-to-all plan and the P receive buffers in this GPU's memory.
+ * Token t sits on device src_part[t] (the s-TS predicted partition), or on the
+ * contiguous split floor(t P / T) when src_part is NULL; pair (t, k) goes to device
+ * expert_part[topk_idx[t, k]]. Receive rows are sorted by (dst, src, t, k): the P
+ * receive buffers are concatenated, device 0 first, each holding its sources'
+ * segments in source order, each segment in the source's (t, k) order -- what an
+ * all2allv delivers from send buffers laid out by (dst, t, k).
+ *   topk_idx    [T, K] int32 in [0, E)
+ *   src_part    nullable [T] int32 in [0, P)
+ *   expert_part [E] int32 in [0, P)
+ *   x           nullable [T, d] dtype (needed when x_recv is given)
+ *   send_counts [P, P] int32: pairs from device p (row) to device q (column); the
+ *               diagonal are the pairs that stay local (the alpha count of the same
+ *               sources); every off-diagonal pair moves d elements each way
+ *   recv_off    [P*P + 1] int32: segment (dst q, src p) is rows
+ *               recv_off[q P + p] .. recv_off[q P + p + 1]
+ *   pair_recv   [T, K] int32: receive row of pair (t, k); passing it as pair_row to
+ *               smoe_combine with the expert outputs in receive order gives the
+ *               combine after the return all-to-all
+ *   recv_token  [T K] int32: token of each receive row
+ *   x_recv      nullable [T K, d] dtype: x_recv[r] = x[recv_token[r]]
+ * P <= 32. Out-of-range indices or map entries are counted as device 0 / expert 0 and
+ * recorded in the status word.                                                        */
+SMOE_API int smoe_ep_exchange(const smoe_desc* desc, const int32_t* topk_idx,
+                              const int32_t* src_part, const int32_t* expert_part,
+                              const void* x, int32_t* send_counts, int32_t* recv_off,
+                              int32_t* pair_recv, int32_t* recv_token, void* x_recv, void* ws,
+                              size_t ws_bytes, void* stream);
+
+/* Shuffled reduce-scatter, SRS ("Speculative MoE" §3.1: the tensor-parallel all-reduce
+ * after attention is replaced by a reduce-scatter that also moves each token to the
+ * device predicted for it). x_shuf[s] = sum_{r=0}^{R-1} x_parts[r][shuf_perm[s]],
+ * added in fp32 in rank order and written in the layer dtype; device p's share is slots
+ * part_off[p] .. part_off[p+1] of the shuffle.
+ *   x_parts   [R, T, d] dtype, the R partial sums; 1 <= R <= 64
+ *   shuf_perm [T] int32 slot -> token (smoe_predict_shuffle's output)
+ *   x_shuf    [T, d] dtype                                                          */
+SMOE_API int smoe_srs(const smoe_desc* desc, int R, const void* x_parts,
+                      const int32_t* shuf_perm, void* x_shuf, void* ws, size_t ws_bytes,
+                      void* stream);
+
+/* Shuffled all-gather, SAG ("Speculative MoE" §3.1: the way back to token order):
+ * y[shuf_perm[s]] = y_shuf[s].
+ *   y_shuf [T, d] dtype in slot order, shuf_perm [T] int32 (a permutation), y [T, d].
+ * A shuf_perm entry out of range is skipped and recorded in the status word.       */
+SMOE_API int smoe_sag(const smoe_desc* desc, const void* y_shuf, const int32_t* shuf_perm,
+                      void* y, void* ws, size_t ws_bytes, void* stream);
 
 /* a9 -- combine ("Speculative MoE" §1: results return to the token's source;
  * FoE: per-group results are summed): y[t] = sum_{k=0}^{K-1} w[t,k] y_disp[pair_row[t,k]]

@@ -63,6 +63,9 @@ SIGNATURES = {
                                               _SZ, _P]),
     "smoe_expert_ffn_gather_fused": (ctypes.c_int, [_D]),
     "smoe_combine": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "smoe_ep_exchange": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "smoe_srs": (ctypes.c_int, [_D, ctypes.c_int, _P, _P, _P, _P, _SZ, _P]),
+    "smoe_sag": (ctypes.c_int, [_D, _P, _P, _P, _P, _SZ, _P]),
     "smoe_layer_forward": (ctypes.c_int, [_D, ctypes.POINTER(LayerWeights),
                                           ctypes.POINTER(LayerIO), _P, _SZ, _P]),
     "smoe_layer_forward_host": (ctypes.c_int, [_D, ctypes.POINTER(LayerWeights), _P, _P, _P, _P,
@@ -224,6 +227,26 @@ def smoe_combine(desc, y_disp, pair_row, topk_w, y_out, ws, y_shared=None, strea
     _check(lib().smoe_combine(ctypes.byref(desc), _ptr(y_disp), _ptr(pair_row), _ptr(topk_w),
                               _ptr(y_shared), _ptr(y_out), _ptr(ws), ws.numel(), _stream(stream)),
            "smoe_combine")
+
+
+def smoe_ep_exchange(desc, topk_idx, expert_part, send_counts, recv_off, pair_recv, recv_token,
+                     ws, src_part=None, x=None, x_recv=None, stream=None):
+    _check(lib().smoe_ep_exchange(ctypes.byref(desc), _ptr(topk_idx), _ptr(src_part),
+                                  _ptr(expert_part), _ptr(x), _ptr(send_counts), _ptr(recv_off),
+                                  _ptr(pair_recv), _ptr(recv_token), _ptr(x_recv), _ptr(ws),
+                                  ws.numel(), _stream(stream)), "smoe_ep_exchange")
+
+
+def smoe_srs(desc, x_parts, shuf_perm, x_shuf, ws, stream=None):
+    """x_parts [R, T, d]; R is taken from its leading dimension."""
+    _check(lib().smoe_srs(ctypes.byref(desc), int(x_parts.shape[0]), _ptr(x_parts),
+                          _ptr(shuf_perm), _ptr(x_shuf), _ptr(ws), ws.numel(), _stream(stream)),
+           "smoe_srs")
+
+
+def smoe_sag(desc, y_shuf, shuf_perm, y, ws, stream=None):
+    _check(lib().smoe_sag(ctypes.byref(desc), _ptr(y_shuf), _ptr(shuf_perm), _ptr(y), _ptr(ws),
+                          ws.numel(), _stream(stream)), "smoe_sag")
 
 
 def layer_weights(w_gate, w1, w3, w2, conf, expert_part) -> LayerWeights:

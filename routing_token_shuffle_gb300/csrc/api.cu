@@ -122,7 +122,9 @@ bool ws_layout(const smoe_desc& d, WsLayout* L) {
   const size_t b = elem_size(d), dm = (size_t)d.d, F = (size_t)d.F, S = (size_t)d.n_shared;
   const size_t tile = (size_t)dispatch_sort_tile(d);
   const size_t ntT = (T + kShufHistTokens - 1) / kShufHistTokens, ntTK = (T * K + tile - 1) / tile;
-  const size_t hist_n = std::max(P * ntT, E * ntTK) + 1;
+  const size_t tile_x = (size_t)exchange_sort_tile(d);
+  const size_t ntX = (T * K + tile_x - 1) / tile_x;      // EP exchange: P^2 buckets
+  const size_t hist_n = std::max(std::max(P * ntT, E * ntTK), P * P * ntX) + 1;
   L->status = take(256);
   L->sort_hist = take(4 * hist_n);
   L->sort_off = take(4 * hist_n);
@@ -404,6 +406,67 @@ SMOE_API int smoe_combine(const smoe_desc* desc, const void* y_disp, const int32
   cudaError_t e = launch_combine(*desc, y_disp, pair_row, topk_w, y_shared, y_out, ws,
                                  static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  return SMOE_OK;
+}
+
+SMOE_API int smoe_ep_exchange(const smoe_desc* desc, const int32_t* topk_idx,
+                              const int32_t* src_part, const int32_t* expert_part,
+                              const void* x, int32_t* send_counts, int32_t* recv_off,
+                              int32_t* pair_recv, int32_t* recv_token, void* x_recv, void* ws,
+                              size_t ws_bytes, void* stream) {
+  SMOE_CHECK(check_desc(desc));
+  SMOE_PTR(topk_idx);
+  SMOE_PTR(expert_part);
+  SMOE_OPT_PTR(src_part);
+  SMOE_PTR(send_counts);
+  SMOE_PTR(recv_off);
+  SMOE_PTR(pair_recv);
+  SMOE_PTR(recv_token);
+  SMOE_OPT_PTR(x_recv);
+  if (x_recv) SMOE_PTR(x);
+  SMOE_CHECK(check_ws(desc, ws, ws_bytes));
+  SMOE_CHECK(check_device());
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (desc->T == 0) {
+    const int P = desc->P;
+    SMOE_CUDA(cudaMemsetAsync(recv_off, 0, sizeof(int32_t) * (P * P + 1), s));
+    SMOE_CUDA(cudaMemsetAsync(send_counts, 0, sizeof(int32_t) * P * P, s));
+    return SMOE_OK;
+  }
+  cudaError_t e = launch_ep_exchange(*desc, topk_idx, src_part, expert_part, x, send_counts,
+                                     recv_off, pair_recv, recv_token, x_recv, ws, s);
+  if (e != cudaSuccess) return cuda_fail(e, "EP exchange launch");
+  return SMOE_OK;
+}
+
+SMOE_API int smoe_srs(const smoe_desc* desc, int R, const void* x_parts,
+                      const int32_t* shuf_perm, void* x_shuf, void* ws, size_t ws_bytes,
+                      void* stream) {
+  SMOE_CHECK(check_desc(desc));
+  SMOE_REQUIRE(R >= 1 && R <= 64, SMOE_ERR_SHAPE, "R=%d must be in [1, 64]", R);
+  SMOE_PTR(x_parts);
+  SMOE_PTR(shuf_perm);
+  SMOE_PTR(x_shuf);
+  SMOE_CHECK(check_ws(desc, ws, ws_bytes));
+  SMOE_CHECK(check_device());
+  if (desc->T == 0) return SMOE_OK;
+  cudaError_t e = launch_srs(*desc, R, x_parts, shuf_perm, x_shuf, ws,
+                             static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "SRS launch");
+  return SMOE_OK;
+}
+
+SMOE_API int smoe_sag(const smoe_desc* desc, const void* y_shuf, const int32_t* shuf_perm,
+                      void* y, void* ws, size_t ws_bytes, void* stream) {
+  SMOE_CHECK(check_desc(desc));
+  SMOE_PTR(y_shuf);
+  SMOE_PTR(shuf_perm);
+  SMOE_PTR(y);
+  SMOE_CHECK(check_ws(desc, ws, ws_bytes));
+  SMOE_CHECK(check_device());
+  if (desc->T == 0) return SMOE_OK;
+  cudaError_t e = launch_sag(*desc, y_shuf, shuf_perm, y, ws, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "SAG launch");
   return SMOE_OK;
 }
 

@@ -98,6 +98,9 @@ constexpr int kSortTile = 1024;     // largest tile (pairs) of the dispatch coun
 // 1024 while the tiles still fit two waves of a 152-SM GPU and the (expert, tile) table
 // stays within four rounds of the scan, so that small batches spread over more SMs.
 int dispatch_sort_tile(const smoe_desc& d);
+// Tile of the expert-parallel exchange's counting sort over P^2 (dst, src) buckets, chosen
+// by the same rule with P^2 buckets.
+int exchange_sort_tile(const smoe_desc& d);
 constexpr int kShufTile = 256;      // tokens per tile of the workspace-free shuffle's sort
 constexpr int kShufHistTokens = 32; // tokens per histogram column of the shuffle sort
 constexpr int kMaxGroups = 520;     // E + n_shared upper bound
@@ -247,6 +250,16 @@ bool ffn_gather_in_gemm(const smoe_desc& d);
 cudaError_t launch_gather_rows(const smoe_desc& d, const void* src, const int32_t* map,
                                int nrows, int nsrc, void* dst, void* ws, cudaStream_t s);
 
+// Expert-parallel exchange plan and receive rows (sort.cu).
+cudaError_t launch_ep_exchange(const smoe_desc& d, const int32_t* idx, const int32_t* src_part,
+                               const int32_t* emap, const void* x, int32_t* send_counts,
+                               int32_t* recv_off, int32_t* pair_recv, int32_t* recv_token,
+                               void* x_recv, void* ws, cudaStream_t s);
+// Shuffled reduce-scatter of R partials into slot order, and its inverse all-gather.
+cudaError_t launch_srs(const smoe_desc& d, int R, const void* x_parts, const int32_t* perm,
+                       void* x_shuf, void* ws, cudaStream_t s);
+cudaError_t launch_sag(const smoe_desc& d, const void* y_shuf, const int32_t* perm, void* y,
+                       void* ws, cudaStream_t s);
 cudaError_t launch_combine(const smoe_desc& d, const void* y_disp, const int32_t* pair_row,
                            const float* w, const void* y_sh, void* y, void* ws, cudaStream_t s);
 

@@ -15,6 +15,8 @@
 #include <algorithm>
 #include <mutex>
 
+#include <cuda.h>
+
 #include "smoe_internal.cuh"
 
 namespace smoe {
@@ -288,7 +290,7 @@ scan_kernel(const int32_t* __restrict__ hist, int32_t* __restrict__ offs, int L,
 // offset of its first column.
 enum ScatterMode { kShuffle = 0, kDispatch = 1 };
 
-template <int MODE>
+template <int MODE, int MAXB = kMaxBuckets>
 __global__ void __launch_bounds__(kThreads)
 scatter_kernel(const int32_t* __restrict__ bucket, int n, int B, int ntiles, int tile,
                int col_stride, const int32_t* __restrict__ offs,
@@ -298,8 +300,8 @@ scatter_kernel(const int32_t* __restrict__ bucket, int n, int B, int ntiles, int
                const int32_t* __restrict__ perm_in, int T, int K, int32_t* __restrict__ pair_row,
                int32_t* __restrict__ row_token, int32_t* __restrict__ row_src) {
   pdl_wait_and_trigger();
-  __shared__ int s_run[kMaxBuckets];
-  __shared__ int s_wc[kWarps][kMaxBuckets];
+  __shared__ int s_run[MAXB];
+  __shared__ int s_wc[kWarps][MAXB];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int b = tid; b < B; b += kThreads) {
     s_run[b] = offs[b * ntiles + blockIdx.x * col_stride];
@@ -377,6 +379,156 @@ gather_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
       const uint4 a = __ldg(in + v), b = __ldg(in + v + 32), c = __ldg(in + v + 64),
                   d = __ldg(in + v + 96);
       out[v] = a; out[v + 32] = b; out[v + 64] = c; out[v + 96] = d;
+    }
+    for (; v < vec_per_row; v += 32) out[v] = __ldg(in + v);
+  }
+}
+
+// ------------------------------------------------------------------ EP exchange
+// "Speculative MoE" §1: under expert parallelism a token travels from its device to
+// the devices of its K experts. Pairs q = t K + k in token order are bucketed by
+// (dst device, src device): bucket = dst P + src, dst = map[idx[t, k]], src =
+// src_part[t] or the contiguous split floor(t P / T). A stable counting sort over
+// these P^2 buckets lays the pairs out as P concatenated receive buffers (device 0
+// first), each holding its sources' segments in source order and, inside a segment,
+// the source's (t, k) order.
+constexpr int kMaxExchangeBuckets = 1024;   // P <= 32
+
+__global__ void __launch_bounds__(kThreads)
+exchange_hist_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ src_part,
+                     const int32_t* __restrict__ emap, int T, int K, int E, int P,
+                     int32_t* __restrict__ bucket, int32_t* __restrict__ hist, int ntiles,
+                     int tile, DeviceStatus* st) {
+  pdl_wait_and_trigger();
+  __shared__ int s_cnt[kMaxExchangeBuckets];
+  __shared__ int s_map[kMaxBuckets];
+  const int tid = threadIdx.x;
+  const int B = P * P;
+  for (int b = tid; b < B; b += kThreads) s_cnt[b] = 0;
+  for (int e = tid; e < E; e += kThreads) {
+    const int p = emap[e];
+    const bool ok = (unsigned)p < (unsigned)P;
+    if (!ok && blockIdx.x == 0) record_error(st, kStatusData, kBadExpertPart, e);
+    s_map[e] = ok ? p : 0;
+  }
+  __syncthreads();
+  // T K <= INT_MAX / 2 (checked on the host)
+  const int n = T * K;
+  const int q0 = blockIdx.x * tile;
+  const int q1 = min(q0 + tile, n);
+#pragma unroll 4
+  for (int q = q0 + tid; q < q1; q += kThreads) {
+    const int t = q / K;
+    int src;
+    if (src_part) {
+      src = src_part[t];
+      if ((unsigned)src >= (unsigned)P) {
+        record_error(st, kStatusData, kBadSrcPart, t);
+        src = 0;
+      }
+    } else {
+      src = (int)(((long long)t * P) / T);
+    }
+    int e = idx[q];
+    if ((unsigned)e >= (unsigned)E) {
+      record_error(st, kStatusData, kBadTopkIdx, q);
+      e = 0;
+    }
+    const int b = s_map[e] * P + src;
+    bucket[q] = b;
+    atomicAdd(&s_cnt[b], 1);
+  }
+  __syncthreads();
+  for (int b = tid; b < B; b += kThreads) hist[b * ntiles + blockIdx.x] = s_cnt[b];
+}
+
+// send_counts[p P + q] = pairs from device p to device q: the length of receive
+// segment (dst q, src p).
+__global__ void __launch_bounds__(kThreads)
+send_counts_kernel(const int32_t* __restrict__ recv_off, int P, int32_t* __restrict__ counts) {
+  pdl_wait_and_trigger();
+  for (int i = threadIdx.x; i < P * P; i += kThreads) {
+    const int p = i / P, q = i - p * P;
+    counts[i] = recv_off[q * P + p + 1] - recv_off[q * P + p];
+  }
+}
+
+// SRS ("Speculative MoE" §3.1): x_shuf[s] = sum_r x_parts[r][perm[s]], the R
+// tensor-parallel partials added in fp32 in rank order and written in slot order.
+// One warp per output row, 16-byte vectors, up to four ranks' loads in flight.
+template <typename TE>
+__global__ void __launch_bounds__(kThreads)
+srs_kernel(const uint4* __restrict__ parts, uint4* __restrict__ out,
+           const int32_t* __restrict__ perm, int T, int R, int vec_per_row,
+           DeviceStatus* st) {
+  pdl_wait_and_trigger();
+  constexpr int V = Elem<TE>::kPerVec16;
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * kThreads + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * kThreads) >> 5;
+  const size_t plane = (size_t)T * vec_per_row;
+  for (int srow = gw; srow < T; srow += nw) {
+    const int t = perm[srow];
+    uint4* o = out + (size_t)srow * vec_per_row;
+    if ((unsigned)t >= (unsigned)T) {
+      if (lane == 0) record_error(st, kStatusData, kBadPerm, srow);
+      for (int v = lane; v < vec_per_row; v += 32) o[v] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const uint4* in = parts + (size_t)t * vec_per_row;
+    for (int v = lane; v < vec_per_row; v += 32) {
+      float acc[V];
+#pragma unroll
+      for (int j = 0; j < V; ++j) acc[j] = 0.0f;
+      int r = 0;
+      for (; r + 4 <= R; r += 4) {
+        uint4 u[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) u[i] = __ldg(in + (size_t)(r + i) * plane + v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float f[V];
+          unpack16(u[i], f, (const TE*)nullptr);
+#pragma unroll
+          for (int j = 0; j < V; ++j) acc[j] += f[j];
+        }
+      }
+      for (; r < R; ++r) {
+        float f[V];
+        unpack16(__ldg(in + (size_t)r * plane + v), f, (const TE*)nullptr);
+#pragma unroll
+        for (int j = 0; j < V; ++j) acc[j] += f[j];
+      }
+      o[v] = pack16(acc, (const TE*)nullptr);
+    }
+  }
+}
+
+// SAG ("Speculative MoE" §3.1): rows held in slot order back to token order,
+// dst[perm[s]] = src[s]; one warp per row, eight 16-byte loads in flight per lane.
+__global__ void __launch_bounds__(kThreads)
+scatter_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                    const int32_t* __restrict__ perm, int nrows, int vec_per_row,
+                    DeviceStatus* st) {
+  pdl_wait_and_trigger();
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * kThreads + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * kThreads) >> 5;
+  for (int r = gw; r < nrows; r += nw) {
+    const int t = perm[r];
+    if ((unsigned)t >= (unsigned)nrows) {
+      if (lane == 0) record_error(st, kStatusData, kBadPerm, r);
+      continue;
+    }
+    const uint4* in = src + (size_t)r * vec_per_row;
+    uint4* out = dst + (size_t)t * vec_per_row;
+    int v = lane;
+    for (; v + 224 < vec_per_row; v += 256) {
+      uint4 u[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) u[i] = __ldg(in + v + 32 * i);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) out[v + 32 * i] = u[i];
     }
     for (; v < vec_per_row; v += 32) out[v] = __ldg(in + v);
   }
@@ -595,6 +747,73 @@ cudaError_t launch_gather_rows(const smoe_desc& d, const void* src, const int32_
   return cudaGetLastError();
 }
 
+int exchange_sort_tile(const smoe_desc& d) {
+  constexpr long long kWaveTiles = 2 * 152;
+  constexpr long long kMaxTable = 4 * 4096;
+  const long long n = (long long)d.T * d.K, B = (long long)d.P * d.P;
+  int tile = kSortTile;
+  while (tile > 256) {
+    const long long nt = (n + tile / 2 - 1) / (tile / 2);
+    if (nt > kWaveTiles || nt * B > kMaxTable) break;
+    tile /= 2;
+  }
+  return tile;
+}
+
+cudaError_t launch_ep_exchange(const smoe_desc& d, const int32_t* idx, const int32_t* src_part,
+                               const int32_t* emap, const void* x, int32_t* send_counts,
+                               int32_t* recv_off, int32_t* pair_recv, int32_t* recv_token,
+                               void* x_recv, void* ws, cudaStream_t s) {
+  WsLayout L;
+  ws_layout(d, &L);
+  DeviceStatus* st = ws_ptr<DeviceStatus>(ws, L.status);
+  int32_t* hist = ws_ptr<int32_t>(ws, L.sort_hist);
+  int32_t* offs = ws_ptr<int32_t>(ws, L.sort_off);
+  int32_t* rows = ws_ptr<int32_t>(ws, L.row_src);        // row -> pair index (unused here)
+  int32_t* bucket = rows + (size_t)d.T * d.K;
+  const int n = d.T * d.K, B = d.P * d.P;
+  const int tile = exchange_sort_tile(d);
+  const int ntiles = ceil_div(n, tile);
+  SMOE_LAUNCH(exchange_hist_kernel, ntiles, kThreads, 0, s, idx, src_part, emap, d.T, d.K, d.E,
+      d.P, bucket, hist, ntiles, tile, st);
+  SMOE_LAUNCH(scan_kernel, 1, 1024, 0, s, hist, offs, B * ntiles, B, ntiles, n, recv_off);
+  SMOE_LAUNCH((scatter_kernel<kDispatch, kMaxExchangeBuckets>), ntiles, kThreads, 0, s, bucket,
+      n, B, ntiles, tile, 1, offs, nullptr, nullptr, d.T, d.K, pair_recv, recv_token, rows);
+  SMOE_LAUNCH(send_counts_kernel, 1, kThreads, 0, s, recv_off, d.P, send_counts);
+  if (x_recv) {
+    const int vec = (int)(d.d * elem_size(d) / 16);
+    SMOE_LAUNCH(gather_rows_kernel, grid_for_rows(n), kThreads, 0, s,
+        static_cast<const uint4*>(x), static_cast<uint4*>(x_recv), recv_token, n, d.T, vec, st);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_srs(const smoe_desc& d, int R, const void* x_parts, const int32_t* perm,
+                       void* x_shuf, void* ws, cudaStream_t s) {
+  WsLayout L;
+  ws_layout(d, &L);
+  DeviceStatus* st = ws_ptr<DeviceStatus>(ws, L.status);
+  const int vec = (int)(d.d * elem_size(d) / 16);
+  if (d.dtype == SMOE_F32)
+    SMOE_LAUNCH(srs_kernel<float>, grid_for_rows(d.T), kThreads, 0, s,
+        static_cast<const uint4*>(x_parts), static_cast<uint4*>(x_shuf), perm, d.T, R, vec, st);
+  else
+    SMOE_LAUNCH(srs_kernel<__nv_bfloat16>, grid_for_rows(d.T), kThreads, 0, s,
+        static_cast<const uint4*>(x_parts), static_cast<uint4*>(x_shuf), perm, d.T, R, vec, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sag(const smoe_desc& d, const void* y_shuf, const int32_t* perm, void* y,
+                       void* ws, cudaStream_t s) {
+  WsLayout L;
+  ws_layout(d, &L);
+  const int vec = (int)(d.d * elem_size(d) / 16);
+  SMOE_LAUNCH(scatter_rows_kernel, grid_for_rows(d.T), kThreads, 0, s,
+      static_cast<const uint4*>(y_shuf), static_cast<uint4*>(y), perm, d.T, vec,
+      ws_ptr<DeviceStatus>(ws, L.status));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_token_cluster(const smoe_desc& d, const int32_t* idx, const int32_t* emap,
                                  int32_t* cluster, void* ws, cudaStream_t s) {
   WsLayout L;
@@ -621,12 +840,12 @@ cudaError_t launch_lar(const smoe_desc& d, const int32_t* idx, const int32_t* sr
 }  // namespace smoe
 
 // ------------------------------------------------------------------ no-allocation variant
-// Some callers cannot allocate device memory at all: code that runs inside a CUDA
-// graph being captured, allocator-free embedded runtimes, or hosts whose memory
-// pool is owned by another framework. For them the predict + shuffle step also
-// exists without a caller workspace: its per-tile histogram and offsets live in
-// the file-scope array below, which every GPU that loads the library keeps until
-// the process exits.
+// Some callers cannot allocate device memory at all: allocator-free embedded
+// runtimes that reserve every byte at start-up, or hosts whose device memory pool
+// is owned by another framework and may not be drawn from. For them the predict +
+// shuffle step also exists without a caller workspace: its per-tile histogram and
+// offsets live in the file-scope array below, which every GPU that loads the
+// library keeps until the process exits.
 namespace smoe {
 namespace {
 
@@ -634,26 +853,68 @@ constexpr int kNoAllocMaxTiles = 4096;                        // T <= 4096 * kSh
 constexpr int kNoAllocScratchInts = 2 * 32 * kNoAllocMaxTiles;  // hist + offs for P <= 32
 static __device__ __align__(256) int32_t g_shuffle_scratch[kNoAllocScratchInts];
 
-// Device address of g_shuffle_scratch per device, looked up once per device with
-// that device current (host code must not use the symbol itself as a pointer).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current CUDA context (0 if there is none yet).
+// Context ids are never reused within a process, so a context created after a reset
+// of the device's primary context has a new id.
+bool current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  if (get_current == nullptr || get_id == nullptr) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return false;
+  *id = 0;
+  return ctx == nullptr || get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of g_shuffle_scratch in the current device's current context. It is
+// looked up with that device current the first time a context calls, and again
+// whenever the device's context has changed since (after cudaDeviceReset the module
+// is loaded anew and the array can move). Host code must not use the symbol itself
+// as a pointer.
 int32_t* noalloc_scratch_ptr(int* err) {
   static std::mutex mu;
   static int32_t* ptrs[64] = {nullptr};
+  static unsigned long long ctx_ids[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess || dev < 0 || dev >= 64) {
     *err = set_last_error(SMOE_ERR_CUDA, "cudaGetDevice failed in the no-allocation shuffle");
     return nullptr;
   }
+  unsigned long long id = 0;
+  if (!current_context_id(&id)) {
+    *err = set_last_error(SMOE_ERR_CUDA, "the current CUDA context could not be queried");
+    return nullptr;
+  }
   std::lock_guard<std::mutex> lock(mu);
-  if (ptrs[dev] == nullptr) {
+  if (ptrs[dev] == nullptr || id == 0 || id != ctx_ids[dev]) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_shuffle_scratch);
+    e = cudaGetSymbolAddress(&p, g_shuffle_scratch);   // makes the context current too
     if (e != cudaSuccess || p == nullptr) {
       *err = set_last_error(SMOE_ERR_CUDA, "cudaGetSymbolAddress of the shuffle scratch failed");
       return nullptr;
     }
+    if (id == 0 && !current_context_id(&id)) {
+      *err = set_last_error(SMOE_ERR_CUDA, "the current CUDA context could not be queried");
+      return nullptr;
+    }
     ptrs[dev] = static_cast<int32_t*>(p);
+    ctx_ids[dev] = id;
   }
   return ptrs[dev];
 }

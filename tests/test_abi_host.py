@@ -183,3 +183,27 @@ def test_binding_refuses_strided_views(lib):
     with pytest.raises(ValueError, match="not contiguous"):
         B.smoe_combine(d, y_disp.t().contiguous(), pair_row, topk_w, y_out, ws, stream=0)
     assert B._ptr(y_out[3:7]) == y_out.data_ptr() + 3 * 64 * 4   # a row range stays dense
+
+
+def test_exchange_srs_sag_validate_on_the_host(lib):
+    """The expert-parallel exchange, SRS and SAG reject missing, misaligned or badly sized
+    arguments before any CUDA call."""
+    d = base_desc()
+    n = B.workspace_size(d)
+    D = ctypes.byref(d)
+    # smoe_ep_exchange(desc, idx, src_part, map, x, send_counts, recv_off, pair_recv,
+    #                  recv_token, x_recv, ws, ws_bytes, stream)
+    assert lib.smoe_ep_exchange(D, None, None, 16, None, 16, 16, 16, 16, None, 256, n, None) == -1
+    assert lib.smoe_ep_exchange(D, 16, 16 + 4, 16, None, 16, 16, 16, 16, None, 256, n,
+                                None) == -3
+    assert lib.smoe_ep_exchange(D, 16, None, 16, None, 16, 16, 16, 16, 16, 256, n, None) == -1
+    assert lib.smoe_ep_exchange(D, 16, None, 16, None, 16, 16, 16, 16, None, 256, n - 1,
+                                None) == -4
+    # smoe_srs(desc, R, x_parts, perm, x_shuf, ws, ws_bytes, stream)
+    assert lib.smoe_srs(D, 0, 16, 16, 16, 256, n, None) == -2
+    assert lib.smoe_srs(D, 65, 16, 16, 16, 256, n, None) == -2
+    assert lib.smoe_srs(D, 2, 16, None, 16, 256, n, None) == -1
+    assert lib.smoe_srs(D, 2, 16, 16, 16 + 8, 256, n, None) == -3
+    # smoe_sag(desc, y_shuf, perm, y, ws, ws_bytes, stream)
+    assert lib.smoe_sag(D, 16, 16, None, 256, n, None) == -1
+    assert lib.smoe_sag(D, 16, 16, 16, None, n, None) == -4

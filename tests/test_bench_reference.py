@@ -1,6 +1,7 @@
 """bench.py's reference arm (the CPU oracle on the host's cores) keeps the JSON-line
 contract and runs on rank 0 only. It needs no GPU, so it is checked here on the CPU
-with the smallest workload."""
+with the smallest workload. It is a pure host process: it never imports the package's
+binding, never maps libsmoe.so and never creates a CUDA context."""
 import json
 import os
 import subprocess
@@ -9,12 +10,6 @@ import sys
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 ARGS = ["--impl", "reference", "--workload", "tiny_fp32", "--steps", "2", "--warmup", "3",
         "--cpu-seconds", "1"]
-
-
-def setup_module():
-    # the workload's descriptor helpers live in the C library (host calls only)
-    from routing_token_shuffle_gb300 import build
-    build.build()
 
 
 def _run(env_extra):
@@ -49,3 +44,20 @@ def test_reference_arm_other_ranks_exit_quietly():
     r = _run({"RANK": "1", "LOCAL_RANK": "1", "WORLD_SIZE": "2"})
     assert r.returncode == 0, r.stderr[-2000:]
     assert not [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+
+
+def test_reference_arm_never_touches_the_library():
+    code = ("import sys, runpy\n"
+            f"sys.argv = ['bench.py'] + {ARGS!r}\n"
+            "runpy.run_path('bench.py', run_name='__main__')\n"
+            "mods = [m for m in sys.modules if m.endswith('binding')]\n"
+            "assert not mods, mods\n"
+            "maps = open('/proc/self/maps').read()\n"
+            "assert 'libsmoe' not in maps\n"
+            "import torch\n"
+            "assert not torch.cuda.is_initialized()\n"
+            "print('clean')\n")
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0 and "clean" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]

@@ -51,7 +51,7 @@ def test_oracle_depends_on_numpy_scipy_and_the_standard_library_only():
 def test_bench_uses_the_oracle_only_in_its_baseline_legs():
     path = os.path.join(ROOT, "bench.py")
     tree = ast.parse(open(path).read(), path)
-    allowed = {"cpu_oracle_rate", "run_reference", "__init__"}
+    allowed = {"cpu_oracle_rate", "run_reference", "reference_inputs"}
     found = []
 
     def visit(node, stack):
@@ -69,12 +69,6 @@ def test_bench_uses_the_oracle_only_in_its_baseline_legs():
     visit(tree, [])
     assert found, "bench.py's baseline legs import the oracle"
     assert all(fn in allowed for _, fn in found), found
-    # inside Workload.__init__ the import sits under the reference arm's switch
-    src = open(path).read().splitlines()
-    for line, fn in found:
-        if fn == "__init__":
-            ctx = "\n".join(src[max(0, line - 3):line])
-            assert "if prepare_with_oracle" in ctx, ctx
 
 
 def test_missing_library_raises():

@@ -1,7 +1,8 @@
 """The workspace-free shuffle entry point, for callers that cannot allocate device
-memory (inside CUDA graph capture, allocator-free runtimes, pools owned by another
-framework). It must return exactly what the workspace entry point returns, call
-after call, although all calls share one library-held scratch array.
+memory (runtimes that reserve all their device memory at start-up and forbid
+allocation afterwards, hosts whose memory pool belongs to another framework). It must
+return exactly what the workspace entry point returns, call after call, although all
+calls share one library-held scratch array, and what the oracle's definition gives.
 
 Kept in its own file, collected last, so a run that stops at the first failure has
 already run every other test; it also passes alone in a fresh process."""
@@ -85,3 +86,45 @@ def test_noalloc_at_the_token_limit(smoe):
         assert torch.equal(r, g)
     off = ref[2].cpu().numpy()
     assert off[0] == 0 and off[-1] == T and (np.diff(off) >= 0).all()
+
+
+def test_noalloc_matches_the_oracle(smoe):
+    # the predicted partitions and the stable shuffle straight from their definitions
+    import oracle as O
+    T, d, E, P, V = 3001, 64, 160, 8, 2000
+    desc = smoe.make_desc(T, d, E, 6, 1, 64, 0, P, V, "bf16")
+    ids, conf, emap, x = make_inputs(11, T, d, E, P, V)
+    i32 = dict(dtype=torch.int32, device="cuda")
+    pred, perm, off = torch.empty(T, **i32), torch.empty(T, **i32), torch.empty(P + 1, **i32)
+    xs = torch.empty_like(x)
+    for _ in range(2):
+        smoe.smoe_predict_shuffle_noalloc(desc, ids, conf, emap, pred, perm, off, x=x, x_shuf=xs)
+        torch.cuda.synchronize()
+        want_pred = O.predict_partition(ids.cpu().numpy(), conf.cpu().numpy(),
+                                        emap.cpu().numpy(), P)
+        want_perm, want_off = O.token_shuffle(want_pred, P)
+        assert np.array_equal(pred.cpu().numpy(), want_pred)
+        assert np.array_equal(perm.cpu().numpy(), want_perm)
+        assert np.array_equal(off.cpu().numpy(), want_off)
+        assert torch.equal(xs, x[perm.long()])
+
+
+def test_noalloc_without_rows_and_with_no_tokens(smoe):
+    # x_shuf = None through the Python wrapper: indices only
+    T, d, E, P, V = 777, 64, 8, 2, 300
+    desc = smoe.make_desc(T, d, E, 2, 1, 64, 0, P, V, "bf16")
+    ws = smoe.workspace(desc)
+    ids, conf, emap, x = make_inputs(5, T, d, E, P, V)
+    ref, _ = run_both(smoe, desc, ids, conf, emap, x, ws)
+    i32 = dict(dtype=torch.int32, device="cuda")
+    pred, perm, off = (torch.full((T,), -3, **i32), torch.full((T,), -3, **i32),
+                       torch.full((P + 1,), -3, **i32))
+    smoe.smoe_predict_shuffle_noalloc(desc, ids, conf, emap, pred, perm, off)
+    torch.cuda.synchronize()
+    assert torch.equal(pred, ref[0]) and torch.equal(perm, ref[1]) and torch.equal(off, ref[2])
+    # T = 0: nothing to predict, every partition offset is zero
+    desc0 = smoe.make_desc(0, d, E, 2, 1, 64, 0, P, V, "bf16")
+    off0 = torch.full((P + 1,), -3, **i32)
+    smoe.smoe_predict_shuffle_noalloc(desc0, ids, conf, emap, pred, perm, off0)
+    torch.cuda.synchronize()
+    assert off0.cpu().tolist() == [0] * (P + 1)
