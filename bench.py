@@ -421,6 +421,55 @@ def speculative_execution_report(wl):
             "routed_forward_ms": round(e0.elapsed_time(e1) / 5, 4)}
 
 
+def ep_exchange_report(wl):
+    """The expert-parallel exchange P devices would run for this batch (outside the timed
+    step): the plan and the receive rows built on this GPU with the s-TS sources, its time
+    and achieved bandwidth, and the bytes that would cross links each way. Then SRS and
+    SAG with two tensor-parallel partials (x and a copy)."""
+    import torch
+    s, c = wl.smoe, wl.cfg
+    dev = wl.dev
+    T, K, P, b = c.T, c.K, c.P, c.elem_bytes
+    i32 = dict(dtype=torch.int32, device=dev)
+    sc, ro = torch.empty(P, P, **i32), torch.empty(P * P + 1, **i32)
+    pr, rt = torch.empty(T, K, **i32), torch.empty(T * K, **i32)
+    xr = wl.x_disp  # T K rows: reused as the receive buffer
+
+    def once():
+        s.smoe_ep_exchange(wl.desc, wl.idx, wl.emap_d, sc, ro, pr, rt, wl.ws, src_part=wl.pred,
+                           x=wl.x, x_recv=xr)
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    once()
+    ev[0].record()
+    for _ in range(10):
+        once()
+    ev[1].record()
+    torch.cuda.synchronize()
+    ms = ev[0].elapsed_time(ev[1]) / 10
+    counts = sc.cpu().numpy()
+    local = int(counts.trace())
+    moved = 2 * T * K * c.d * b + T * K * 12 + T * K * 4
+    parts = torch.stack([wl.x, wl.x])
+    xs, yb = torch.empty_like(wl.x), torch.empty_like(wl.x)
+    s.smoe_srs(wl.desc, parts, wl.perm, xs, wl.ws)
+    s.smoe_sag(wl.desc, xs, wl.perm, yb, wl.ws)
+    ev2 = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    ev2[0].record()
+    for _ in range(10):
+        s.smoe_srs(wl.desc, parts, wl.perm, xs, wl.ws)
+    ev2[1].record()
+    for _ in range(10):
+        s.smoe_sag(wl.desc, xs, wl.perm, yb, wl.ws)
+    ev2[2].record()
+    torch.cuda.synchronize()
+    srs_ms, sag_ms = ev2[0].elapsed_time(ev2[1]) / 10, ev2[1].elapsed_time(ev2[2]) / 10
+    return {"ms": round(ms, 4), "GB/s": round(moved / (ms / 1e3) / 1e9, 1),
+            "local_pairs": local, "remote_pairs": int(T * K - local),
+            "link_bytes_each_way": int((T * K - local) * c.d * b),
+            "srs_R2_ms": round(srs_ms, 4), "sag_ms": round(sag_ms, 4)}
+
+
 def placement_report(wl):
     """Offline s-EG placement: co-cluster the profile batch's token-expert activations
     (cross-entropy optimisation, seeded) and measure, on this batch, α and the imbalance
@@ -482,11 +531,18 @@ def cpu_oracle_rate(h: HostLayer, target_s: float, max_tokens: int | None = None
                         H=cfg.H, P=cfg.P, n_shared=cfg.n_shared)
         return time.perf_counter() - t0
 
-    n = min(cap, 16)
-    t = run(n)
-    while t < target_s / 4 and n < cap:
-        n = min(cap, max(n * 2, int(n * target_s / max(t, 1e-3) * 0.8)))
-        t = run(n)
+    # time = a + b n: a fixed part per call (the oracle converts every expert's weights to
+    # float64 on each call) plus a part per token; two sizes fix both, then n is chosen so
+    # that one call takes about target_s
+    n0, n1 = min(cap, 16), min(cap, 128)
+    t0 = run(n0)
+    n, t = n0, t0
+    if n1 > n0:
+        t1 = run(n1)
+        b = max((t1 - t0) / (n1 - n0), 1e-9)
+        a = max(t0 - b * n0, 0.0)
+        n = int(max(n0, min(cap, (target_s - a) / b)))
+        t = t1 if n == n1 else run(n)
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     return n / t, n, t, cores
 
@@ -752,6 +808,7 @@ def run_native(args):
         result["alpha"]["sTS_with_table_A"] = inter_info["alpha_sTS_inter"]
         result["stages"]["predict_shuffle_inter (outside the step)"] = {
             "ms": inter_info["predict_shuffle_inter_ms"]}
+    result["ep_exchange"] = ep_exchange_report(wl)
     if not args.no_placement:
         result["placement"] = placement_report(wl)
     if cfg.H > 1:
