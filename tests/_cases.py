@@ -86,3 +86,16 @@ def sample_tokens(T, n=48, seed=0):
     pick = set(rng.choice(T, size=min(n, T), replace=False).tolist())
     pick.update({0, T - 1})
     return np.array(sorted(pick))
+
+
+def block_edge_rows(offsets, block=64):
+    """First and last row of every `block`-row block of every segment [offsets[e],
+    offsets[e+1]): one row per CTA half of every GEMM tile, whatever the tile shape (256-row
+    pair tiles, 128-row tiles, 64-row halves of a 128-row pair tail), in every wave of a
+    persistent schedule."""
+    rows = set()
+    for lo, hi in zip(offsets[:-1], offsets[1:]):
+        for b in range(int(lo), int(hi), block):
+            rows.add(b)
+            rows.add(min(b + block - 1, int(hi) - 1))
+    return np.array(sorted(rows), dtype=np.int64)

@@ -14,7 +14,7 @@ import oracle as O
 import routing_token_shuffle_gb300 as smoe
 from routing_token_shuffle_gb300 import synth
 
-from _cases import Case, rel_err_rows, sample_tokens, to_np
+from _cases import Case, block_edge_rows, rel_err_rows, sample_tokens, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -364,10 +364,11 @@ def test_expert_ffn_and_combine(name, T):
     smoe.smoe_combine(desc, yd, pr, w, y, ws, y_shared=ysh)
     smoe.smoe_get_status(ws)
     torch.cuda.synchronize()
-    # expert outputs on sampled rows (the last row of every expert segment included)
+    # expert outputs on sampled rows plus the first and last row of every 64-row block of
+    # every expert segment: both CTAs of every tile, every wave of the persistent schedule
     eo_n, rt_n, idx_n = to_np(eo), to_np(rt), to_np(idx)
     rows = set(sample_tokens(TK, 48, seed=1).tolist())
-    rows.update(int(eo_n[e + 1] - 1) for e in range(cfg.E) if eo_n[e + 1] > eo_n[e])
+    rows.update(block_edge_rows(eo_n).tolist())
     rows = np.array(sorted(rows))
     row_exp = np.searchsorted(eo_n, rows, side="right") - 1
     ref = np.zeros((len(rows), cfg.d))
@@ -376,7 +377,7 @@ def test_expert_ffn_and_combine(name, T):
         ref[sel] = O.swiglu_ffn(c.x_np[rt_n[rows[sel]]], *c.expert_weights_np(int(e)))
     assert rel_err_rows(to_np(yd)[rows], ref).max() <= VALUE_TOL
     if cfg.n_shared:
-        toks = sample_tokens(cfg.T, 16, seed=2)
+        toks = np.union1d(sample_tokens(cfg.T, 16, seed=2), block_edge_rows([0, cfg.T]))
         for j in range(cfg.n_shared):
             rj = O.swiglu_ffn(c.x_np[toks], *c.expert_weights_np(cfg.E + j))
             assert rel_err_rows(to_np(ysh[j])[toks], rj).max() <= VALUE_TOL
@@ -416,8 +417,15 @@ def test_layer_forward(name, T):
         assert np.array_equal(to_np(outs[k]), ref), k
     assert np.array_equal(to_np(outs["lar"]).astype(np.uint64),
                           O.lar_counts(idx, c.emap, cfg.P, cfg.H, src_part=pred))
-    # values against the oracle's own routing, tokens near a routing tie excluded
-    toks = np.arange(cfg.T) if cfg.T <= 1024 else sample_tokens(cfg.T, 40, seed=4)
+    # values against the oracle's own routing, tokens near a routing tie excluded; at large
+    # T a sample plus the tokens of the first and last row of every 64-row block of every
+    # expert segment and of the shared experts' rows (every tile of both GEMMs)
+    if cfg.T <= 1024:
+        toks = np.arange(cfg.T)
+    else:
+        toks = np.union1d(sample_tokens(cfg.T, 40, seed=4), rt[block_edge_rows(eo)])
+        if cfg.n_shared:
+            toks = np.union1d(toks, block_edge_rows([0, cfg.T]))
     own_logits = O.gate_logits(c.x_np[toks], to_np(c.w_gate))
     margin = O.selection_margin(own_logits, cfg.K, cfg.H)
     keep = margin >= MARGIN
