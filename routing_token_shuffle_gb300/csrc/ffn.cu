@@ -155,7 +155,8 @@ struct Tile {
   int b_row;          // first B row
   long long out_row;  // first output row (in out, or in out_sh for a shared down tile)
   bool out_shared;
-  bool m128;          // two-SM tile of 128 rows (64 per CTA): a group's last <= 128 rows
+  bool swap;          // two-SM tile of a group's last <= 128 rows with swapped operands
+  int N;              // MMA N: 256, or the swapped tile's tokens rounded up to 32
 };
 
 template <bool UP>
@@ -456,9 +457,15 @@ __device__ __forceinline__ bool wait_rows(const GemmArgs& p, int lo, int hi, vol
 // B halves: up, 64 W1 rows then the same 64 W3 rows (leader: features n0 .. n0+63,
 // peer: n0+64 .. n0+127), so that every accumulator row holds the gate and the up value
 // of each of its features; down, the leader's and the peer's 128 of the 256 W2 rows.
-// A group whose last rows fit in 128 ends with an M = 128 tile: 64 A rows per CTA, and
-// the accumulator of a CTA holds its 64 rows x the first N/2 columns in lanes 0-63 and
-// x the last N/2 columns in lanes 64-127 (TMEM columns 0 .. N/2-1 in both cases).
+// A group whose last rows fit in 128 ends with a swapped tile: the 256 MMA rows are the
+// weight rows that would have been B (each CTA's own 128, loaded exactly as B) and the
+// N = 32 .. 128 columns are the group's last tokens (N/2 per CTA, loaded with the 64-row
+// box), so the tile's MMA work follows its tokens. An M = 128 two-SM MMA keeps the tensor
+// pipes as busy as an M = 256 one (measured: every k-block of a 128-row tail took as long
+// as a full tile's on the DeepSeek-V2-shaped layer, where 87 of 338 row tiles are tails).
+// The accumulator of a swapped tile is transposed: TMEM lane = weight row (up: lanes 0-63
+// the gate and 64-127 the up value of the CTA's 64 features; down: the CTA's 128 output
+// columns), TMEM column = token; its epilogue writes the output token by token.
 // The leader's thread issues the MMAs; stage bytes of both CTAs complete on the leader's
 // `full` barrier; MMA completion is multicast to both CTAs' `empty` and `tfull`; both
 // epilogues drain their own TMEM lanes and arrive on the leader's `tempty`.
@@ -486,8 +493,11 @@ __device__ __forceinline__ void decode_pair_tile(const int32_t* ts, const int32_
   const int j = g - p.E;
   r.g = g;
   r.rows = shared ? p.T : eo[g + 1] - eo[g];
-  r.m128 = r.rows - m_pair * 256 <= 128;
-  r.m0 = m_pair * 256 + (int)rank * (r.m128 ? 64 : 128);
+  const int rem = r.rows - m_pair * 256;
+  r.swap = rem <= 128;
+  r.N = r.swap ? (rem + 31) & ~31 : 256;
+  // this CTA's first operand row: its 128 of a 256-row tile, or its N/2 of the tokens
+  r.m0 = m_pair * 256 + (int)rank * (r.swap ? r.N / 2 : 128);
   if (UP) {
     r.n0 = n_tile * 128;
     r.a_shared = shared;
@@ -516,7 +526,6 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,     // 128-row
   pdl_wait_and_trigger();
   using TE = __nv_bfloat16;
   constexpr uint32_t kIdesc = tc::instr_desc(false, 256, 256);
-  constexpr uint32_t kIdesc128 = tc::instr_desc(false, 128, 256);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -578,11 +587,12 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,     // 128-row
     for (int t = pair; t < total && ok; t += npairs) {
       Tile tl;
       decode_pair_tile<UP>(s_ts, s_eo, p, t, rank, tl);
-      const CUtensorMap* amap = tl.m128 ? (tl.a_shared ? &tmA_sh64 : &tmA64)
+      // token rows: 128 (256-row tile) or a 64-row box holding the CTA's N/2 <= 64 tokens
+      const CUtensorMap* amap = tl.swap ? (tl.a_shared ? &tmA_sh64 : &tmA64)
                                         : (tl.a_shared ? &tmA_sh : &tmA);
-      const uint32_t tx = 2 * ((tl.m128 ? kPairStage / 2 : kPairStage) + kPairStage);
+      const uint32_t tx = 2 * ((tl.swap ? kPairStage / 2 : kPairStage) + kPairStage);
       if (UP && p.g_src && !tl.a_shared &&
-          !wait_rows(p, tl.a_row, min(tl.a_row + (tl.m128 ? 64 : 128), s_eo[tl.g + 1]), abort)) {
+          !wait_rows(p, tl.a_row, min(tl.a_row + (tl.swap ? 64 : 128), s_eo[tl.g + 1]), abort)) {
         ok = false;
         break;
       }
@@ -608,7 +618,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,     // 128-row
     for (int t = pair; t < total && ok; t += npairs, ++tcount) {
       Tile tl;
       decode_pair_tile<UP>(s_ts, s_eo, p, t, rank, tl);
-      const uint32_t idesc = tl.m128 ? kIdesc128 : kIdesc;
+      // swapped tile: the weight rows (B stage) are the MMA's A, the tokens its B
+      const uint32_t idesc = tl.swap ? tc::instr_desc(false, 256, tl.N) : kIdesc;
       const uint32_t a = tcount & 1u, aph = (tcount >> 1) & 1u;
       if (!tc::mbar_wait(&tempty[a], aph ^ 1u, abort)) { ok = false; break; }
       tc::fence_after_sync();
@@ -617,8 +628,10 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,     // 128-row
         const uint32_t s = it % kPairStages, ph = (it / kPairStages) & 1u;
         if (!tc::mbar_wait(&full[s], ph, abort)) { ok = false; break; }
         tc::fence_after_sync();
-        const uint64_t adesc = tc::sw128_kmajor_desc(tc::smem_u32(sA + s * kPairStage));
-        const uint64_t bdesc = tc::sw128_kmajor_desc(tc::smem_u32(sB + s * kPairStage));
+        const uint64_t tok_desc = tc::sw128_kmajor_desc(tc::smem_u32(sA + s * kPairStage));
+        const uint64_t w_desc = tc::sw128_kmajor_desc(tc::smem_u32(sB + s * kPairStage));
+        const uint64_t adesc = tl.swap ? w_desc : tok_desc;
+        const uint64_t bdesc = tl.swap ? tok_desc : w_desc;
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           tc::mma_bf16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc,
@@ -652,13 +665,62 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,     // 128-row
         break;
       }
       tc::fence_after_sync();
-      // This warp's TMEM lanes: for M = 256, rows 32q .. 32q+31 of the CTA's 128 over all
-      // N columns; for M = 128, rows 32 (q & 1) .. of the CTA's 64 over the N columns of
-      // half (q >> 1), in TMEM columns 0 .. 127.
-      const int rsub = tl.m128 ? (q & 1) : q;
-      const int nhalf = tl.m128 ? (q >> 1) : 0;
-      const int ncols = tl.m128 ? 128 : 256;
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + a * kAccCols;
+      if (tl.swap) {
+        // TMEM column c = token t0 + c of the tile (the leader's N/2 tokens, then the
+        // peer's); this warp's lanes are weight rows 32q .. 32q + 31 of the CTA's 128
+        const int half = tl.N >> 1;
+        const int ntok = tl.rows - (tl.m0 - (int)rank * half);    // tokens in the tile
+        const long long row0 = tl.out_row - (long long)rank * half;  // output row of t0
+        TE* out = static_cast<TE*>(tl.out_shared ? p.out_sh : p.out);
+        float* xchg = reinterpret_cast<float*>(sOut);  // up values [64 features][33]
+        // the exchange buffer overlaps the staging rows of warps 0-2: every epilogue warp
+        // has finished the previous tile's stores before any of it is overwritten
+        if (UP) asm volatile("bar.sync 1, 128;" ::: "memory");
+#pragma unroll 1
+        for (int c0 = 0; c0 < tl.N; c0 += 32) {
+          uint32_t v[32];
+          tc::tmem_ld32(taddr + c0, v);
+          tc::tmem_ld_wait();
+          if (c0 + 32 >= tl.N) {  // read out: the next tile's MMAs may start
+            tc::fence_before_sync();
+            tc::mbar_arrive_cluster(tc::cluster_addr(&tempty[a], 0));
+          }
+          if (UP) {
+            // warps 2-3 hold the up values of the features whose gates warps 0-1 hold
+            if (q >= 2) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) xchg[((q - 2) * 32 + lane) * 33 + i] = __uint_as_float(v[i]);
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (q < 2) {
+              const int col = tl.n0 + 64 * (int)rank + 32 * q + lane;
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const int tk = c0 + i;
+                const float gg = __uint_as_float(v[i]);
+                const float h = gg / (1.0f + __expf(-gg)) * xchg[(q * 32 + lane) * 33 + i];
+                if (tk < ntok && col < p.N)
+                  out[(size_t)(row0 + tk) * p.N + col] = Elem<TE>::from_f32(h);
+              }
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+          } else {
+            const int col = tl.n0 + 128 * (int)rank + 32 * q + lane;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int tk = c0 + i;
+              if (tk < ntok && col < p.N)
+                out[(size_t)(row0 + tk) * p.N + col] = Elem<TE>::from_f32(__uint_as_float(v[i]));
+            }
+          }
+        }
+        continue;
+      }
+      // rows 32q .. 32q+31 of the CTA's 128 over all 256 columns
+      const int rsub = q;
+      const int nhalf = 0;
+      const int ncols = 256;
       const RowStager<TE> rs{sOut + q * 4096, static_cast<TE*>(tl.out_shared ? p.out_sh : p.out),
                              tl.out_row + rsub * 32, clamp_rows(tl.rows - tl.m0 - rsub * 32),
                              p.N};

@@ -590,12 +590,13 @@ def test_expert_ffn_two_sm_tiles_ragged(T, E, K, S, d, F):
 
 @pytest.mark.parametrize("d,F", [(384, 704), (256, 256)])
 def test_expert_ffn_two_sm_tail_tiles(d, F):
-    """Two-SM tiles end a group with an M = 128 tile (64 rows per CTA) when its last rows
-    fit in 128 and with a full 256-row tile otherwise. Expert segments of 64, 300, 450, 0,
-    129, 128, 513 and 257 rows hit every case (a group that is only an M = 128 tile, M =
-    128 tails of 44, 1 and 1 rows, a 194-row M = 256 tail, a 129-row group, an empty
-    group), and the shared expert's 1100 rows end in a 76-row M = 128 tail; F = 704 and
-    d = 384 leave half-valid last n-tiles in the up and the down GEMM."""
+    """Two-SM tiles end a group with a swapped tile (weight rows as the MMA's 256 rows, the
+    group's last tokens as its N = 32 .. 128 columns) when its last rows fit in 128 and
+    with a full 256-row tile otherwise. Expert segments of 64, 300, 450, 0, 129, 128, 513
+    and 257 rows hit every case (a group that is only a swapped tile, swapped tails of 44,
+    1 and 1 rows, a 128-row swapped group, a 194-row M = 256 tail, a 129-row group, an
+    empty group), and the shared expert's 1100 rows end in a 76-row swapped tail; F = 704
+    and d = 384 leave half-valid last n-tiles in the up and the down GEMM."""
     counts = [64, 300, 450, 0, 129, 128, 513, 257]
     E, K, S, T = len(counts), 2, 1, 1100
     assert T * K >= 256 * E and sum(counts) <= T * K
