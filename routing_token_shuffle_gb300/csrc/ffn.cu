@@ -469,11 +469,15 @@ __device__ __forceinline__ bool wait_rows(const GemmArgs& p, int lo, int hi, vol
 // The leader's thread issues the MMAs; stage bytes of both CTAs complete on the leader's
 // `full` barrier; MMA completion is multicast to both CTAs' `empty` and `tfull`; both
 // epilogues drain their own TMEM lanes and arrive on the leader's `tempty`.
-constexpr int kPairStages = 6;
+// Ring of kPairStages stages, each two 64-wide k-blocks deep (A and B: 2 x 16 KB per CTA),
+// so that a barrier round trip and a commit serve 8 MMAs: measured against 6 single
+// k-block stages, the FFN took 3 % less time on the Mixtral shape, 2.5 % on the Qwen3
+// shape and 0.4 % on the DeepSeek-V2 shape.
+constexpr int kPairStages = 3;
 // warps 0-7 as in the single-SM kernel; warps 2, 3 and 8-11 copy rows in gather mode
 constexpr int kPairThreads = 384;
 constexpr uint32_t kPairStage = 128 * 128;  // A half or B half: 128 rows x 128 bytes
-constexpr size_t kPairSmemBytes = 1024 + kPairStages * 2 * kPairStage + kStageOut + 256 +
+constexpr size_t kPairSmemBytes = 1024 + kPairStages * 4 * kPairStage + kStageOut + 256 +
                                   4 * (kMaxGroups + 1 + 513 + 4);
 
 template <bool UP>
@@ -531,8 +535,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,     // 128-row
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = base;
-  uint8_t* sB = base + kPairStages * kPairStage;
-  uint8_t* sOut = sB + kPairStages * kPairStage;
+  uint8_t* sB = base + 2 * kPairStages * kPairStage;
+  uint8_t* sOut = sB + 2 * kPairStages * kPairStage;
   uint64_t* full = reinterpret_cast<uint64_t*>(sOut + kStageOut);
   uint64_t* empty = full + kPairStages;
   uint64_t* tfull = empty + kPairStages;
@@ -596,15 +600,19 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,     // 128-row
         ok = false;
         break;
       }
-      for (int kb = 0; kb < nkb; ++kb, ++it) {
+      for (int kb2 = 0; kb2 < nkb; kb2 += 2, ++it) {
         const uint32_t s = it % kPairStages, ph = (it / kPairStages) & 1u;
+        const int nj = min(2, nkb - kb2);
         if (!tc::mbar_wait(&empty[s], ph ^ 1u, abort)) { ok = false; break; }
         const uint32_t leader_full = tc::cluster_addr(&full[s], 0);
-        if (rank == 0) tc::mbar_expect_tx(&full[s], tx);
-        uint8_t* b = sB + s * kPairStage;
-        tc::tma_load_2d_pair(sA + s * kPairStage, amap, leader_full, kb * 64, tl.a_row);
-        tc::tma_load_2d_pair(b, &tmB1, leader_full, kb * 64, tl.b_row);
-        if (UP) tc::tma_load_2d_pair(b + kPairStage / 2, &tmB3, leader_full, kb * 64, tl.b_row);
+        if (rank == 0) tc::mbar_expect_tx(&full[s], tx * nj);
+        for (int j = 0; j < nj; ++j) {
+          const int kb = kb2 + j;
+          uint8_t* b = sB + (s * 2 + j) * kPairStage;
+          tc::tma_load_2d_pair(sA + (s * 2 + j) * kPairStage, amap, leader_full, kb * 64, tl.a_row);
+          tc::tma_load_2d_pair(b, &tmB1, leader_full, kb * 64, tl.b_row);
+          if (UP) tc::tma_load_2d_pair(b + kPairStage / 2, &tmB3, leader_full, kb * 64, tl.b_row);
+        }
       }
     }
     if (!ok) {
@@ -624,18 +632,21 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,     // 128-row
       if (!tc::mbar_wait(&tempty[a], aph ^ 1u, abort)) { ok = false; break; }
       tc::fence_after_sync();
       const uint32_t d_tmem = tmem + a * kAccCols;
-      for (int kb = 0; kb < nkb; ++kb, ++it) {
+      for (int kb2 = 0; kb2 < nkb; kb2 += 2, ++it) {
         const uint32_t s = it % kPairStages, ph = (it / kPairStages) & 1u;
+        const int nj = min(2, nkb - kb2);
         if (!tc::mbar_wait(&full[s], ph, abort)) { ok = false; break; }
         tc::fence_after_sync();
-        const uint64_t tok_desc = tc::sw128_kmajor_desc(tc::smem_u32(sA + s * kPairStage));
-        const uint64_t w_desc = tc::sw128_kmajor_desc(tc::smem_u32(sB + s * kPairStage));
-        const uint64_t adesc = tl.swap ? w_desc : tok_desc;
-        const uint64_t bdesc = tl.swap ? tok_desc : w_desc;
+        for (int j = 0; j < nj; ++j) {
+          const uint64_t tok_desc = tc::sw128_kmajor_desc(tc::smem_u32(sA + (s * 2 + j) * kPairStage));
+          const uint64_t w_desc = tc::sw128_kmajor_desc(tc::smem_u32(sB + (s * 2 + j) * kPairStage));
+          const uint64_t adesc = tl.swap ? w_desc : tok_desc;
+          const uint64_t bdesc = tl.swap ? tok_desc : w_desc;
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          tc::mma_bf16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc,
-                            (kb > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < 4; ++k)
+            tc::mma_bf16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc,
+                              (kb2 + j > 0 || k > 0) ? 1u : 0u);
+        }
         tc::commit_pair(&empty[s], 0x3);
       }
       if (!ok) break;
