@@ -916,6 +916,8 @@ cudaError_t launch_route_fused(const smoe_desc& d, int rows, const void* x, cons
   if (d.E <= 32) return launch_fused<8, 4>(tX, tW, a, tiles, smem, s);
   if (d.E <= 64) return launch_fused<8, 8>(tX, tW, a, tiles, smem, s);
   if (d.E <= 128) return launch_fused<8, 16>(tX, tW, a, tiles, smem, s);
+  // 16 lanes per token and only the value slots the experts fill (E = 160: 10 of 16)
+  if (d.E <= 160) return launch_fused<16, 10>(tX, tW, a, tiles, smem, s);
   return launch_fused<16, 16>(tX, tW, a, tiles, smem, s);
 }
 
@@ -1009,6 +1011,11 @@ cudaError_t launch_route(const smoe_desc& d, int rows, const void* x, const void
     else
       SMOE_LAUNCH((select_sub_kernel<8, 16>), grid, 256, 0, s, part, KS, stride, lo, rows, d.E,
                   d.K, d.H, d.renorm, topk_idx, topk_w, so);
+    return cudaGetLastError();
+  }
+  if (d.K <= 16 && d.E <= 160) {
+    SMOE_LAUNCH((select_sub_kernel<16, 10>), ceil_div(rows * 16, 256), 256, 0, s, part, KS,
+                stride, lo, rows, d.E, d.K, d.H, d.renorm, topk_idx, topk_w, so);
     return cudaGetLastError();
   }
   if (d.K <= 16 && d.E <= 256) {
