@@ -543,6 +543,9 @@ def cpu_oracle_rate(h: HostLayer, target_s: float, max_tokens: int | None = None
         a = max(t0 - b * n0, 0.0)
         n = int(max(n0, min(cap, (target_s - a) / b)))
         t = t1 if n == n1 else run(n)
+        if t < target_s / 2 and n < cap:   # the fit undershot: scale by the measured rate
+            n = int(min(cap, max(n + 1, (n * (target_s - a) / max(t - a, 1e-3)) * 0.9)))
+            t = run(n)
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     return n / t, n, t, cores
 
