@@ -666,14 +666,29 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,     // 128-row
     // ---------------------------------------------------------------- epilogue (both CTAs)
     const int q = warp & 3;
     uint32_t tcount = 0;
+    bool failed = false;
     for (int t = pair; t < total; t += npairs, ++tcount) {
       Tile tl;
       decode_pair_tile<UP>(s_ts, s_eo, p, t, rank, tl);
       const uint32_t a = tcount & 1u, aph = (tcount >> 1) & 1u;
-      if (!tc::mbar_wait(&tfull[a], aph, abort)) {
+      // A warp whose wait fails does not leave the loop: the swapped up epilogue
+      // synchronises the four epilogue warps on named barrier 1, so a failed warp keeps
+      // taking part in those barriers (and does nothing else) while the others, seeing
+      // the abort flag, fail their own waits at once.
+      if (!failed && !tc::mbar_wait(&tfull[a], aph, abort)) {
         *abort = 1;
         record_error(p.st, kStatusTimeout, kTimeoutGemm, blockIdx.x);
-        break;
+        failed = true;
+      }
+      if (failed) {
+        if (UP && tl.swap) {
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+          for (int c0 = 0; c0 < tl.N; c0 += 32) {
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+          }
+        }
+        continue;
       }
       tc::fence_after_sync();
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + a * kAccCols;
