@@ -328,7 +328,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       Tile tl;
       decode_tile<UP>(s_ts, s_eo, p, t, tl);
       const uint32_t a = tcount & 1u, aph = (tcount >> 1) & 1u;
-      if (!tc::mbar_wait(&tfull[a], aph, abort)) {
+      if (!tc::mbar_wait_warp(&tfull[a], aph, abort)) {
         *abort = 1;
         record_error(p.st, kStatusTimeout, kTimeoutGemm, blockIdx.x);
         break;
@@ -675,7 +675,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,     // 128-row
       // synchronises the four epilogue warps on named barrier 1, so a failed warp keeps
       // taking part in those barriers (and does nothing else) while the others, seeing
       // the abort flag, fail their own waits at once.
-      if (!failed && !tc::mbar_wait(&tfull[a], aph, abort)) {
+      if (!failed && !tc::mbar_wait_warp(&tfull[a], aph, abort)) {
         *abort = 1;
         record_error(p.st, kStatusTimeout, kTimeoutGemm, blockIdx.x);
         failed = true;

@@ -515,7 +515,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
   } else if (warp >= 4) {
     const int q = warp & 3;
     const int r = q * 32 + lane;
-    if (tc::mbar_wait(tfull, 0, abort)) {
+    if (tc::mbar_wait_warp(tfull, 0, abort)) {
       tc::fence_after_sync();
       const int row = m0 + r;
       float* out = p.part + ((size_t)ks * p.rows + row) * p.E;
