@@ -532,9 +532,11 @@ def cpu_oracle_rate(h: HostLayer, target_s: float, max_tokens: int | None = None
         return time.perf_counter() - t0
 
     # time = a + b n: a fixed part per call (the oracle converts every expert's weights to
-    # float64 on each call) plus a part per token; two sizes fix both, then n is chosen so
-    # that one call takes about target_s
+    # float64 on each call) plus a part per token; two sizes fix both (after one untimed
+    # call that takes the one-time costs), then n is chosen so that one call takes about
+    # target_s
     n0, n1 = min(cap, 16), min(cap, 128)
+    run(n0)
     t0 = run(n0)
     n, t = n0, t0
     if n1 > n0:
@@ -543,9 +545,14 @@ def cpu_oracle_rate(h: HostLayer, target_s: float, max_tokens: int | None = None
         a = max(t0 - b * n0, 0.0)
         n = int(max(n0, min(cap, (target_s - a) / b)))
         t = t1 if n == n1 else run(n)
-        if t < target_s / 2 and n < cap:   # the fit undershot: scale by the measured rate
-            n = int(min(cap, max(n + 1, (n * (target_s - a) / max(t - a, 1e-3)) * 0.9)))
-            t = run(n)
+    # the per-token cost falls as n grows (larger matrix products per expert) and the two
+    # small calls fix it poorly, so the fit can undershoot: grow n by the measured rate,
+    # at least doubling it, until one call takes half of target_s (at most four calls)
+    for _ in range(4):
+        if t >= target_s / 2 or n >= cap:
+            break
+        n = int(min(cap, max(2 * n, n * 0.9 * target_s / max(t, 1e-3))))
+        t = run(n)
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     return n / t, n, t, cores
 

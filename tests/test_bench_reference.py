@@ -61,3 +61,40 @@ def test_reference_arm_never_touches_the_library():
     r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True,
                        text=True, timeout=600)
     assert r.returncode == 0 and "clean" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]
+
+
+def test_cpu_oracle_rate_sample_reaches_half_the_target(monkeypatch):
+    """The CPU baseline's sample grows until one oracle call takes at least half of the
+    target seconds (or the whole batch), also when the oracle's cost per token falls as
+    the sample grows (as numpy's matrix products do) and when its first call carries a
+    one-time cost: a fake clock and a fake oracle stand in for both."""
+    import types
+
+    import numpy as np
+
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle as O
+    from routing_token_shuffle_gb300 import synth
+    clock = [0.0]
+    calls = []
+    cost = {}
+
+    def fake_layer_forward(x, *args, **kw):
+        n = len(x)
+        calls.append(n)
+        clock[0] += cost["a"] + cost["c"] * n ** cost["p"] + (cost["first"] if len(calls) == 1 else 0)
+
+    monkeypatch.setattr(bench, "time", types.SimpleNamespace(perf_counter=lambda: clock[0]))
+    monkeypatch.setattr(O, "layer_forward", fake_layer_forward)
+    cfg = synth.CONFIGS["dsv2_prefill"]
+    z = np.zeros((cfg.T, 1), np.float32)
+    h = bench.HostLayer(cfg, z, np.zeros(cfg.T, np.int32), None, None, None, None, None, None)
+    for a_, c_, p_, first in ((0.3, 0.01, 0.8, 0.0), (1.0, 0.05, 0.6, 3.0), (0.2, 0.02, 0.7, 6.0),
+                              (2.5, 0.002, 1.0, 0.0), (0.5, 0.08, 0.5, 1.0)):
+        cost.update(a=a_, c=c_, p=p_, first=first)
+        for target in (4.0, 10.0, 15.0):
+            calls.clear()
+            rate, n, secs, cores = bench.cpu_oracle_rate(h, target)
+            assert (secs >= target / 2 or n == cfg.T) and len(calls) <= 9, (cost, target, n, secs, calls)
+            assert rate == n / secs and cores >= 1
