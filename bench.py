@@ -547,9 +547,9 @@ def cpu_oracle_rate(h: HostLayer, target_s: float, max_tokens: int | None = None
         t = t1 if n == n1 else run(n)
     # the per-token cost falls as n grows (larger matrix products per expert) and the two
     # small calls fix it poorly, so the fit can undershoot: grow n by the measured rate,
-    # at least doubling it, until one call takes half of target_s (at most four calls)
+    # at least doubling it, until one call takes 0.7 of target_s (at most four calls)
     for _ in range(4):
-        if t >= target_s / 2 or n >= cap:
+        if t >= 0.7 * target_s or n >= cap:
             break
         n = int(min(cap, max(2 * n, n * 0.9 * target_s / max(t, 1e-3))))
         t = run(n)

@@ -63,8 +63,8 @@ def test_reference_arm_never_touches_the_library():
     assert r.returncode == 0 and "clean" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]
 
 
-def test_cpu_oracle_rate_sample_reaches_half_the_target(monkeypatch):
-    """The CPU baseline's sample grows until one oracle call takes at least half of the
+def test_cpu_oracle_rate_sample_reaches_most_of_the_target(monkeypatch):
+    """The CPU baseline's sample grows until one oracle call takes at least 0.7 of the
     target seconds (or the whole batch), also when the oracle's cost per token falls as
     the sample grows (as numpy's matrix products do) and when its first call carries a
     one-time cost: a fake clock and a fake oracle stand in for both."""
@@ -96,5 +96,5 @@ def test_cpu_oracle_rate_sample_reaches_half_the_target(monkeypatch):
         for target in (4.0, 10.0, 15.0):
             calls.clear()
             rate, n, secs, cores = bench.cpu_oracle_rate(h, target)
-            assert (secs >= target / 2 or n == cfg.T) and len(calls) <= 9, (cost, target, n, secs, calls)
+            assert (secs >= 0.7 * target or n == cfg.T) and len(calls) <= 9, (cost, target, n, secs, calls)
             assert rate == n / secs and cores >= 1
