@@ -124,14 +124,17 @@ def source_hash(*names) -> str:
 
 def stage_bytes(cfg, rows_in_ffn: bool = False) -> dict:
     """Algorithmic bytes per stage (each input read once, each output written once). With
-    rows_in_ffn the dispatch stage only sorts (indices in, pair_row / row_token / row_slot
-    out) and its row copy runs inside the expert FFN's up GEMM."""
+    rows_in_ffn the shuffle copies x to x_shuf, the dispatch stage only sorts (indices in,
+    pair_row / row_token / row_slot out) and its row copy runs inside the expert FFN's up
+    GEMM; otherwise the shuffle stage computes the permutation alone and the dispatch
+    stage sorts, then writes x_shuf and X_disp from one read of x."""
     T, d, E, K, S, b = cfg.T, cfg.d, cfg.E, cfg.K, cfg.n_shared, cfg.elem_bytes
+    rows = 2 * T * d * b                       # x read, x_shuf written
     return {
         "route": T * d * b + E * d * b + T * E * 4 + T * K * 8,
-        "predict_shuffle": T * 4 + T * E * 4 + 2 * T * d * b + 3 * T * 4,
+        "predict_shuffle": T * 4 + T * E * 4 + 3 * T * 4 + (rows if rows_in_ffn else 0),
         "lar": T * K * 4 + T * 4,
-        "dispatch": (T * K * 16 if rows_in_ffn else 2 * T * K * d * b + T * K * 12),
+        "dispatch": (T * K * 16 if rows_in_ffn else T * K * 12 + T * 4 + rows + T * K * d * b),
         "combine": T * K * d * b + S * T * d * b + T * K * 8 + T * d * b,
     }
 
@@ -345,8 +348,10 @@ class Workload:
         nvtx.range_push(Workload.STAGES[0])
         s.smoe_route(c.desc, c.x, c.w_gate, c.idx, c.w, logits_out=c.logits, ws=c.ws)
         rec(0)
+        # the rows of x_shuf are written here when the FFN copies the dispatched rows
+        # itself, else with the dispatched rows after the dispatch's sort
         s.smoe_predict_shuffle(c.desc, c.ids_d, c.conf_d, c.emap_d, c.pred, c.perm, c.part_off,
-                               c.ws, x=c.x, x_shuf=c.x_shuf)
+                               c.ws, x=c.x, x_shuf=c.x_shuf if c.rows_in_ffn else None)
         rec(1)
         s.smoe_lar(c.desc, c.idx, c.emap_d, c.lar, c.ws, src_part=c.pred)
         rec(2)
@@ -358,8 +363,11 @@ class Workload:
             s.smoe_expert_ffn_gather(c.desc, c.x_shuf, c.row_slot, c.x_disp, c.expert_off, c.w1,
                                      c.w3, c.w2, c.x_disp, c.ws, x=c.x, y_shared=c.y_sh)
         else:
+            # the dispatch sorts; then one pass over x writes x_shuf and the dispatched rows
             s.smoe_dispatch(c.desc, c.idx, c.expert_off, c.pair_row, c.row_token, c.ws,
-                            shuf_perm=c.perm, x_src=c.x_shuf, x_disp=c.x_disp)
+                            shuf_perm=c.perm)
+            s.smoe_shuffle_dispatch_rows(c.desc, c.x, c.pair_row, c.x_disp, c.ws,
+                                         shuf_perm=c.perm, x_shuf=c.x_shuf)
             rec(3)
             s.smoe_expert_ffn(c.desc, c.x_disp, c.expert_off, c.w1, c.w3, c.w2, c.x_disp, c.ws,
                               x=c.x, y_shared=c.y_sh)

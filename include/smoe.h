@@ -7,6 +7,7 @@
  *   C_p lookup -> predicted partition -> shuffle    -> smoe_predict_shuffle
  *   local activation rate alpha                     -> smoe_lar
  *   permute pairs into per-expert contiguous rows   -> smoe_dispatch
+ *   x_shuf and the dispatched rows from one read    -> smoe_shuffle_dispatch_rows
  *   grouped SwiGLU expert FFN                       -> smoe_expert_ffn
  *   dispatch's row copy + expert FFN in one call    -> smoe_expert_ffn_gather
  *   weighted combine back into token order          -> smoe_combine
@@ -207,6 +208,24 @@ SMOE_API int smoe_dispatch(const smoe_desc* desc, const int32_t* topk_idx,
                            const int32_t* shuf_perm, const void* x_src, int32_t* expert_off,
                            int32_t* pair_row, int32_t* row_token, int32_t* row_slot,
                            void* x_disp, void* ws, size_t ws_bytes, void* stream);
+
+/* a4 + a6 -- the shuffle's row copy and the dispatch's row copy from one read of x
+ * ("Speculative MoE" §3.1 s-TS, Fig. 2, and §1 dispatch): for slot s and its token
+ * t = shuf_perm[s] (t = s when shuf_perm is NULL),
+ *   x_shuf[s] = x[t]  and  x_disp[pair_row[t, k]] = x[t] for k < K,
+ * the same rows smoe_predict_shuffle(x_shuf) and smoe_dispatch(x_src = x_shuf, x_disp)
+ * write, with every row of x read once instead of x_shuf being read back K times.
+ *   x          [T, d] dtype
+ *   shuf_perm  nullable [T] int32 slot -> token (smoe_predict_shuffle's output)
+ *   pair_row   [T, K] int32 (smoe_dispatch's output for the same shuf_perm)
+ *   x_shuf     nullable [T, d] dtype (needs shuf_perm)
+ *   x_disp     [T K, d] dtype
+ * A slot whose token is out of range gives a zero x_shuf row; a pair_row entry outside
+ * [0, T K) is skipped; both record SMOE_ERR_DATA.                                    */
+SMOE_API int smoe_shuffle_dispatch_rows(const smoe_desc* desc, const void* x,
+                                        const int32_t* shuf_perm, const int32_t* pair_row,
+                                        void* x_shuf, void* x_disp, void* ws, size_t ws_bytes,
+                                        void* stream);
 
 /* a7/a8 -- grouped SwiGLU expert FFN: for every expert e and each of its rows,
  * y = (silu(x W1_e^T) * (x W3_e^T)) W2_e^T, bf16/tf32 tensor-core products with fp32

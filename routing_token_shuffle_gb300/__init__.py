@@ -17,7 +17,8 @@ _BINDING_NAMES = (
     "smoe_expert_ffn_gather", "smoe_expert_ffn_gather_fused", "smoe_get_status", "smoe_lar",
     "smoe_layer_forward", "smoe_moe_forward_routed", "smoe_layer_forward_host",
     "smoe_predict_shuffle", "smoe_predict_shuffle_inter", "smoe_predict_shuffle_noalloc",
-    "smoe_prefetch_predict", "smoe_route", "smoe_sag", "smoe_selftest_device_timeout", "smoe_srs",
+    "smoe_prefetch_predict", "smoe_route", "smoe_sag", "smoe_selftest_device_timeout",
+    "smoe_shuffle_dispatch_rows", "smoe_srs",
     "smoe_token_cluster", "workspace", "workspace_size",
 )
 

@@ -58,6 +58,7 @@ SIGNATURES = {
     "smoe_predict_shuffle_inter": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                                   _SZ, _P]),
     "smoe_dispatch": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "smoe_shuffle_dispatch_rows": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "smoe_expert_ffn": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "smoe_expert_ffn_gather": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                               _SZ, _P]),
@@ -202,6 +203,14 @@ def smoe_dispatch(desc, topk_idx, expert_off, pair_row, row_token, ws, shuf_perm
                                _ptr(expert_off), _ptr(pair_row), _ptr(row_token), _ptr(row_slot),
                                _ptr(x_disp), _ptr(ws), ws.numel(), _stream(stream)),
            "smoe_dispatch")
+
+
+def smoe_shuffle_dispatch_rows(desc, x, pair_row, x_disp, ws, shuf_perm=None, x_shuf=None,
+                               stream=None):
+    _check(lib().smoe_shuffle_dispatch_rows(ctypes.byref(desc), _ptr(x), _ptr(shuf_perm),
+                                            _ptr(pair_row), _ptr(x_shuf), _ptr(x_disp), _ptr(ws),
+                                            ws.numel(), _stream(stream)),
+           "smoe_shuffle_dispatch_rows")
 
 
 def smoe_expert_ffn(desc, x_disp, expert_off, w1, w3, w2, y_disp, ws, x=None, y_shared=None,

@@ -334,6 +334,27 @@ SMOE_API int smoe_dispatch(const smoe_desc* desc, const int32_t* topk_idx,
   return SMOE_OK;
 }
 
+SMOE_API int smoe_shuffle_dispatch_rows(const smoe_desc* desc, const void* x,
+                                        const int32_t* shuf_perm, const int32_t* pair_row,
+                                        void* x_shuf, void* x_disp, void* ws, size_t ws_bytes,
+                                        void* stream) {
+  SMOE_CHECK(check_desc(desc));
+  SMOE_PTR(x);
+  SMOE_OPT_PTR(shuf_perm);
+  SMOE_PTR(pair_row);
+  SMOE_OPT_PTR(x_shuf);
+  SMOE_PTR(x_disp);
+  SMOE_REQUIRE(x_shuf == nullptr || shuf_perm != nullptr, SMOE_ERR_ARG,
+               "x_shuf needs shuf_perm");
+  SMOE_CHECK(check_ws(desc, ws, ws_bytes));
+  SMOE_CHECK(check_device());
+  if (desc->T == 0) return SMOE_OK;
+  cudaError_t e = launch_shuffle_dispatch_rows(*desc, x, shuf_perm, pair_row, x_shuf, x_disp, ws,
+                                               static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "shuffle/dispatch rows launch");
+  return SMOE_OK;
+}
+
 SMOE_API int smoe_expert_ffn(const smoe_desc* desc, const void* x_disp, const void* x,
                              const int32_t* expert_off, const void* w1, const void* w3,
                              const void* w2, void* y_disp, void* y_shared, void* ws,
@@ -488,25 +509,34 @@ static int layer_forward_impl(const smoe_desc* d, const smoe_layer_weights* W,
   void* y_disp = ws_ptr<char>(ws, L.y_disp);
   void* y_sh = d->n_shared ? ws_ptr<char>(ws, L.y_sh) : nullptr;
 
+  // where the FFN does not copy the dispatched rows inside its up GEMM, one pass over x
+  // writes both x_shuf and X_disp after the dispatch's sort
+  const bool rows_fused = !ffn_gather_in_gemm(*d);
   cudaError_t e = launch_route(*d, d->T, io->x, W->w_gate, nullptr, logits, idx, w, ws, s);
   if (e != cudaSuccess) return cuda_fail(e, "route launch");
   e = launch_predict_shuffle(*d, io->token_ids, W->conf, W->expert_part, io->x, pred, perm,
-                             part_off, io->skip_shuffle ? nullptr : x_shuf, ws, s);
+                             part_off, io->skip_shuffle || rows_fused ? nullptr : x_shuf, ws, s);
   if (e != cudaSuccess) return cuda_fail(e, "predict/shuffle launch");
   if (io->lar) {
     e = launch_lar(*d, idx, pred, W->expert_part, io->lar, ws, s);
     if (e != cudaSuccess) return cuda_fail(e, "lar launch");
   }
   const void* x_src = io->skip_shuffle ? io->x : x_shuf;
-  // the dispatch sorts the pairs; the FFN copies the rows (inside its up GEMM when it
-  // runs two-SM tiles)
+  // the dispatch sorts the pairs; then either one pass over x writes x_shuf and X_disp,
+  // or the FFN copies the rows from x_shuf inside its up GEMM
   int32_t* row_slot = ws_ptr<int32_t>(ws, L.row_src);
-  e = launch_dispatch(*d, idx, io->skip_shuffle ? nullptr : perm, x_src, expert_off, pair_row,
-                      row_token, row_slot, nullptr, ws, s);
+  const int32_t* shuf = io->skip_shuffle ? nullptr : perm;
+  e = launch_dispatch(*d, idx, shuf, x_src, expert_off, pair_row, row_token, row_slot, nullptr,
+                      ws, s);
   if (e != cudaSuccess) return cuda_fail(e, "dispatch launch");
+  if (rows_fused) {
+    e = launch_shuffle_dispatch_rows(*d, io->x, shuf, pair_row, shuf ? x_shuf : nullptr, x_disp,
+                                     ws, s);
+    if (e != cudaSuccess) return cuda_fail(e, "shuffle/dispatch rows launch");
+  }
   const FfnGather g{x_src, row_slot, d->T};
   e = launch_expert_ffn(*d, x_disp, io->x, expert_off, W->w1, W->w3, W->w2, y_disp, y_sh, ws, s,
-                        &g);
+                        rows_fused ? nullptr : &g);
   if (e != cudaSuccess) return cuda_fail(e, "expert ffn launch");
   e = launch_combine(*d, y_disp, pair_row, w, y_sh, io->y, ws, s);
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");

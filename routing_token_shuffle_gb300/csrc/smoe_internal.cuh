@@ -246,6 +246,11 @@ cudaError_t launch_expert_ffn(const smoe_desc& d, const void* x_disp, const void
                               cudaStream_t s, const FfnGather* gather = nullptr);
 // true when launch_expert_ffn with a gather copies the rows inside its up GEMM
 bool ffn_gather_in_gemm(const smoe_desc& d);
+// x_shuf[s] = x[perm[s]] (x_shuf nullable; perm NULL: the identity) and X_disp[pair_row[t,
+// k]] = x[t], from one read of each row of x
+cudaError_t launch_shuffle_dispatch_rows(const smoe_desc& d, const void* x, const int32_t* perm,
+                                        const int32_t* pair_row, void* x_shuf, void* x_disp,
+                                        void* ws, cudaStream_t s);
 // dst[r] = src[map[r]] for nrows rows of d elements (16-byte vectors)
 cudaError_t launch_gather_rows(const smoe_desc& d, const void* src, const int32_t* map,
                                int nrows, int nsrc, void* dst, void* ws, cudaStream_t s);

@@ -384,6 +384,64 @@ gather_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
   }
 }
 
+// The shuffle's row copy and the dispatch's row copy from one read of x ("Speculative
+// MoE" §3.1 s-TS and §1 dispatch): for slot s and its token t = perm[s] (t = s without a
+// shuffle), x_shuf[s] = x[t] and X_disp[pair_row[t, k]] = x[t] for k < K. The rows the
+// dispatch would read back from x_shuf are written while x[t] is in registers. One warp
+// per slot, eight 16-byte loads in flight per lane, each stored to the token's 1 + K rows.
+__global__ void __launch_bounds__(kThreads)
+shuffle_dispatch_rows_kernel(const uint4* __restrict__ x, uint4* __restrict__ x_shuf,
+                             uint4* __restrict__ x_disp, const int32_t* __restrict__ perm,
+                             const int32_t* __restrict__ pair_row, int T, int K, int vec,
+                             DeviceStatus* st) {
+  pdl_wait_and_trigger();
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * kThreads + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * kThreads) >> 5;
+  const int TK = T * K;
+  for (int s = gw; s < T; s += nw) {
+    const int t = perm ? perm[s] : s;
+    uint4* out0 = x_shuf ? x_shuf + (size_t)s * vec : nullptr;
+    if ((unsigned)t >= (unsigned)T) {
+      if (lane == 0) record_error(st, kStatusData, kBadPerm, s);
+      if (out0)
+        for (int v = lane; v < vec; v += 32) out0[v] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    int my_row = -1;  // lane k < K: the dispatched row of pair (t, k)
+    if (lane < K) {
+      const int r = pair_row[(size_t)t * K + lane];
+      if ((unsigned)r < (unsigned)TK)
+        my_row = r;
+      else
+        record_error(st, kStatusData, kBadPairRow, t * K + lane);
+    }
+    const uint4* in = x + (size_t)t * vec;
+    // every lane takes every chunk (the shuffles below span the warp), whatever the row
+    // length; lane + 32 u past the row does nothing
+    for (int c0 = 0; c0 < vec; c0 += 256) {
+      const int v0 = c0 + lane;
+      uint4 tv[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (v0 + 32 * u < vec) tv[u] = __ldg(in + v0 + 32 * u);
+      if (out0) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (v0 + 32 * u < vec) out0[v0 + 32 * u] = tv[u];
+      }
+      for (int k = 0; k < K; ++k) {
+        const int r = __shfl_sync(0xffffffffu, my_row, k);
+        if (r < 0) continue;
+        uint4* o = x_disp + (size_t)r * vec;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (v0 + 32 * u < vec) o[v0 + 32 * u] = tv[u];
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ EP exchange
 // "Speculative MoE" §1: under expert parallelism a token travels from its device to
 // the devices of its K experts. Pairs q = t K + k in token order are bucketed by
@@ -733,6 +791,18 @@ cudaError_t launch_dispatch(const smoe_desc& d, const int32_t* idx, const int32_
     SMOE_LAUNCH(gather_rows_kernel, grid_for_rows(n), kThreads, 0, s,
         static_cast<const uint4*>(x_src), static_cast<uint4*>(x_disp), row_src, n, d.T, vec, st);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_shuffle_dispatch_rows(const smoe_desc& d, const void* x, const int32_t* perm,
+                                        const int32_t* pair_row, void* x_shuf, void* x_disp,
+                                        void* ws, cudaStream_t s) {
+  WsLayout L;
+  ws_layout(d, &L);
+  const int vec = (int)(d.d * elem_size(d) / 16);
+  SMOE_LAUNCH(shuffle_dispatch_rows_kernel, grid_for_rows(d.T), kThreads, 0, s,
+      static_cast<const uint4*>(x), static_cast<uint4*>(x_shuf), static_cast<uint4*>(x_disp),
+      perm, pair_row, d.T, d.K, vec, ws_ptr<DeviceStatus>(ws, L.status));
   return cudaGetLastError();
 }
 

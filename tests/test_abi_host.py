@@ -147,6 +147,21 @@ def test_ffn_gather_validates_on_the_host(lib):
                                       None) == -4
 
 
+def test_shuffle_dispatch_rows_validates_on_the_host(lib):
+    d = base_desc()
+    n = B.workspace_size(d)
+    D = ctypes.byref(d)
+    # smoe_shuffle_dispatch_rows(desc, x, shuf_perm, pair_row, x_shuf, x_disp, ws, ws_bytes,
+    #                            stream)
+    f = lib.smoe_shuffle_dispatch_rows
+    assert f(D, None, 16, 16, 16, 16, 256, n, None) == -1        # x missing
+    assert f(D, 16, 16, None, 16, 16, 256, n, None) == -1        # pair_row missing
+    assert f(D, 16, 16, 16, 16, None, 256, n, None) == -1        # x_disp missing
+    assert f(D, 16, None, 16, 16, 16, 256, n, None) == -1        # x_shuf without shuf_perm
+    assert f(D, 16, 16 + 4, 16, 16, 16, 256, n, None) == -3      # misaligned
+    assert f(D, 16, 16, 16, 16, 16, 256, 16, None) == -4         # workspace too small
+
+
 def test_ffn_gather_fused_query(lib):
     """The row copy runs inside the up GEMM only on bf16 two-SM tiles with F <= 1024: of
     the workloads, the Qwen3-shaped layer (F = 768, 1024 rows per expert)."""

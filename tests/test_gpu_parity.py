@@ -251,6 +251,91 @@ def test_dispatch(name, T):
     assert torch.equal(xd, c.x[torch.as_tensor(r_rt, device="cuda").long()])
 
 
+@pytest.mark.parametrize("name,T", CASES, ids=IDS)
+def test_shuffle_dispatch_rows(name, T):
+    """x_shuf and the dispatched rows written from one read of x: bit for bit the
+    oracle's shuffle (x[perm]) and dispatch (x[row_token]) on the oracle's own
+    permutations, with the shuffle and without it (rows in token order, no x_shuf); a
+    slot with an out-of-range token gives a zero x_shuf row and a pair_row entry out of
+    range is skipped, both reported."""
+    c = get_case(name, T)
+    cfg = c.cfg
+    desc = smoe.desc_from_config(cfg)
+    ws = smoe.workspace(desc)
+    logits, idx, w = run_route(c, desc, ws)
+    pred, perm, off, _ = run_shuffle(c, desc, ws, with_x=False)
+    smoe.smoe_get_status(ws)
+    ref_pred = O.predict_partition(c.ids, c.conf, c.emap, cfg.P)
+    ref_perm, _ = O.token_shuffle(ref_pred, cfg.P)
+    assert np.array_equal(to_np(perm), ref_perm)
+    TK = cfg.T * cfg.K
+    eo, pr, rt = i32(cfg.E + 1), i32(cfg.T, cfg.K), i32(TK)
+    smoe.smoe_dispatch(desc, idx, eo, pr, rt, ws, shuf_perm=perm)
+    r_eo, r_pr, r_rt = O.expert_dispatch(to_np(idx), cfg.E, ref_perm)
+    assert np.array_equal(to_np(pr), r_pr)
+    xsh = torch.full_like(c.x, 5.0)
+    xd = torch.full((TK, cfg.d), 7.0, dtype=c.x.dtype, device="cuda")
+    smoe.smoe_shuffle_dispatch_rows(desc, c.x, pr, xd, ws, shuf_perm=perm, x_shuf=xsh)
+    smoe.smoe_get_status(ws)
+    assert torch.equal(xsh, c.x[torch.as_tensor(ref_perm, device="cuda").long()])
+    assert torch.equal(xd, c.x[torch.as_tensor(r_rt, device="cuda").long()])
+    # without the shuffle: the pairs in token order, no x_shuf
+    smoe.smoe_dispatch(desc, idx, eo, pr, rt, ws)
+    _, r_pr0, r_rt0 = O.expert_dispatch(to_np(idx), cfg.E, None)
+    xd0 = torch.full_like(xd, 3.0)
+    smoe.smoe_shuffle_dispatch_rows(desc, c.x, pr, xd0, ws)
+    smoe.smoe_get_status(ws)
+    assert torch.equal(xd0, c.x[torch.as_tensor(r_rt0, device="cuda").long()])
+    # planted bad entries: a slot's token and one pair's row
+    s_bad, t_bad = cfg.T // 3, int(ref_perm[cfg.T // 2])
+    bad_perm = perm.clone()
+    bad_perm[s_bad] = cfg.T + 7
+    bad_pr = torch.as_tensor(r_pr, device="cuda").clone()
+    r_lost = int(bad_pr[t_bad, 0])
+    bad_pr[t_bad, 0] = -3
+    xsh2, xd2 = torch.full_like(c.x, 5.0), torch.full_like(xd, 7.0)
+    smoe.smoe_shuffle_dispatch_rows(desc, c.x, bad_pr, xd2, ws, shuf_perm=bad_perm, x_shuf=xsh2)
+    with pytest.raises(smoe.SmoeError):
+        smoe.smoe_get_status(ws)
+    assert (xsh2[s_bad] == 0).all()
+    keep_s = torch.ones(cfg.T, dtype=torch.bool, device="cuda")
+    keep_s[s_bad] = False
+    assert torch.equal(xsh2[keep_s], xsh[keep_s])
+    assert (xd2[r_lost] == 7.0).all()                      # the skipped row is untouched
+    t_skip = int(ref_perm[s_bad])                          # that slot's rows were not written
+    lost = {r_lost} | {int(r) for r in r_pr[t_skip]}
+    keep_r = torch.ones(TK, dtype=torch.bool, device="cuda")
+    keep_r[sorted(lost)] = False
+    assert torch.equal(xd2[keep_r], xd[keep_r])
+
+
+@pytest.mark.parametrize("T,d,K,dtype", [(300, 64, 32, "bf16"), (37, 8, 3, "bf16"),
+                                         (129, 200, 5, "bf16"), (64, 256, 1, "f32"),
+                                         (1000, 2056, 7, "bf16")],
+                         ids=["d64-K32", "d8-K3", "d200-K5", "d256f32-K1", "d2056-K7"])
+def test_shuffle_dispatch_rows_row_lengths(T, d, K, dtype):
+    """One read of x for x_shuf and the dispatched rows, at row lengths of 1 to 257
+    16-byte vectors (fewer than a warp's lanes, a ragged last chunk, several chunks) and
+    K up to 32: every x_shuf row is x[perm[s]] and every dispatched row x[t] of its pair,
+    for random permutations of the slots and of the T K rows."""
+    E = 32
+    desc = smoe.make_desc(T, d, E, K, 1, 64, 0, 2, 100, dtype)
+    ws = smoe.workspace(desc)
+    g = torch.Generator(device="cuda").manual_seed(T + d + K)
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    x = torch.randn(T, d, generator=g, device="cuda").to(tdt)
+    perm = torch.randperm(T, generator=g, device="cuda").to(torch.int32)
+    pair_row = torch.randperm(T * K, generator=g, device="cuda").to(torch.int32).view(T, K)
+    xsh = torch.full_like(x, 5.0)
+    xd = torch.full((T * K, d), 7.0, dtype=tdt, device="cuda")
+    smoe.smoe_shuffle_dispatch_rows(desc, x, pair_row, xd, ws, shuf_perm=perm, x_shuf=xsh)
+    smoe.smoe_get_status(ws)
+    assert torch.equal(xsh, x[perm.long()])
+    ref = torch.empty_like(xd)
+    ref[pair_row.long().view(-1)] = x.repeat_interleave(K, dim=0)
+    assert torch.equal(xd, ref)
+
+
 GATHER_CASES = [("tiny_fp32", 37), ("mixtral", 1001), ("dsv2_prefill", 1537), ("dsv2_decode", None),
                 ("qwen3_foe", 3001), ("mixtral", None), ("qwen3_foe", None)]
 
