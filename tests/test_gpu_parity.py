@@ -711,6 +711,48 @@ def test_expert_ffn_two_sm_tail_tiles(d, F):
     assert rel_err_rows(to_np(ysh[0]), O.swiglu_ffn(xn, *W[E])).max() <= VALUE_TOL
 
 
+@pytest.mark.parametrize("counts,S,T", [
+    ([300] * 32, 0, 4800),                       # every group ends in a 44-row tail
+    ([512] * 8, 0, 2048),                        # no tail: two-SM tiles move to the other kernel
+    ([1, 700, 0, 256, 255, 1000, 129, 3, 2000, 44] * 3, 1, 13000)],
+    ids=["all-tails", "no-tails", "ragged-shared"])
+def test_expert_ffn_two_sm_tail_mixes(counts, S, T):
+    """Two-SM tiles on row mixes at the extremes: every group ending in a 44-row swapped
+    tail, no tail at all (whole 256-row tiles only), and ragged groups (1, 3 and 44 rows,
+    255 and 129, empty, multiples of 256) with a shared expert. Every row equals the
+    oracle's expert FFN; rows past the last group are not written."""
+    d, F, K = 256, 256, 2
+    E = len(counts)
+    assert T * K >= 256 * E and sum(counts) <= T * K
+    g = torch.Generator(device="cuda").manual_seed(E + S)
+    x = torch.randn(T, d, generator=g, device="cuda").to(torch.bfloat16)
+    xd = torch.randn(T * K, d, generator=g, device="cuda").to(torch.bfloat16)
+    w1 = (torch.randn(E + S, F, d, generator=g, device="cuda") / d ** 0.5).to(torch.bfloat16)
+    w3 = (torch.randn(E + S, F, d, generator=g, device="cuda") / d ** 0.5).to(torch.bfloat16)
+    w2 = (torch.randn(E + S, d, F, generator=g, device="cuda") / F ** 0.5).to(torch.bfloat16)
+    eo_n = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    eo = torch.as_tensor(eo_n, device="cuda")
+    desc = smoe.make_desc(T, d, E, K, 1, F, S, 2, 100, "bf16")
+    ws = smoe.workspace(desc)
+    yd = torch.full_like(xd, 7.0)
+    ysh = torch.empty(S, T, d, dtype=torch.bfloat16, device="cuda") if S else None
+    smoe.smoe_expert_ffn(desc, xd, eo, w1, w3, w2, yd, ws, x=x, y_shared=ysh)
+    smoe.smoe_get_status(ws)
+    torch.cuda.synchronize()
+    xdn, xn = to_np(xd).astype(np.float64), to_np(x).astype(np.float64)
+    W = [tuple(to_np(m[e]).astype(np.float64) for m in (w1, w3, w2)) for e in range(E + S)]
+    y = to_np(yd)
+    ref = np.zeros_like(xdn)
+    for e in range(E):
+        lo, hi = eo_n[e], eo_n[e + 1]
+        ref[lo:hi] = O.swiglu_ffn(xdn[lo:hi], *W[e])
+    n = eo_n[-1]
+    assert rel_err_rows(y[:n], ref[:n]).max() <= VALUE_TOL
+    assert (y[n:] == 7.0).all()
+    for j in range(S):
+        assert rel_err_rows(to_np(ysh[j]), O.swiglu_ffn(xn, *W[E + j])).max() <= VALUE_TOL
+
+
 @pytest.mark.parametrize("name,T", [("tiny_fp32", None), ("dsv2_prefill", 1537), ("qwen3_foe", 3001),
                                     ("dsv2_prefill", None)],
                          ids=["tiny", "dsv2-T1537", "qwen3-T3001", "dsv2-full"])
