@@ -771,6 +771,10 @@ def run_native(args):
     stages["expert_ffn"]["TFLOP/s"] = round(achieved_tf, 2)
     if wl.rows_in_ffn:
         stages["dispatch"]["rows"] = "sort only; the row copy runs inside the expert_ffn up GEMM"
+    else:
+        stages["dispatch"]["rows"] = ("sort, then one read of x writes x_shuf and the T K "
+                                      "dispatched rows (predict_shuffle computes the "
+                                      "permutation only)")
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
