@@ -546,10 +546,15 @@ def test_layer_forward_host_buffers():
     assert torch.equal(yh, y_dev.cpu())
 
 
-def test_skip_shuffle_is_lossless():
-    """Dispatching without the shuffle gives the same output (the shuffle only moves
-    data: the pages call s-MoE lossless)."""
-    c = get_case("qwen3_foe", 3001)
+@pytest.mark.parametrize("name,T", [("qwen3_foe", 3001), ("dsv2_prefill", 1537), ("mixtral", 1001),
+                                    ("qwen3_foe", None)],
+                         ids=["qwen3-T3001", "dsv2-T1537-shared", "mixtral-T1001", "qwen3-full-two-sm"])
+def test_skip_shuffle_is_lossless(name, T):
+    """Dispatching without the shuffle gives the same output, bit for bit (the shuffle only
+    moves data: the pages call s-MoE lossless): through the one-read row pass for x_shuf
+    and the dispatched rows (the first three), and through the up GEMM's own row copy
+    on two-SM tiles (the full Qwen3-shaped layer)."""
+    c = get_case(name, T)
     cfg = c.cfg
     desc = smoe.desc_from_config(cfg)
     ws = smoe.workspace(desc)
