@@ -155,7 +155,7 @@ struct Tile {
   int b_row;          // first B row
   long long out_row;  // first output row (in out, or in out_sh for a shared down tile)
   bool out_shared;
-  bool swap;          // two-SM tile of a group's last <= 128 rows with swapped operands
+  bool swap;          // two-SM tile of a group's last <= 192 rows with swapped operands
   int N;              // MMA N: 256, or the swapped tile's tokens rounded up to 32
 };
 
@@ -457,12 +457,17 @@ __device__ __forceinline__ bool wait_rows(const GemmArgs& p, int lo, int hi, vol
 // B halves: up, 64 W1 rows then the same 64 W3 rows (leader: features n0 .. n0+63,
 // peer: n0+64 .. n0+127), so that every accumulator row holds the gate and the up value
 // of each of its features; down, the leader's and the peer's 128 of the 256 W2 rows.
-// A group whose last rows fit in 128 ends with a swapped tile: the 256 MMA rows are the
+// A group whose last rows fit in 192 ends with a swapped tile: the 256 MMA rows are the
 // weight rows that would have been B (each CTA's own 128, loaded exactly as B) and the
-// N = 32 .. 128 columns are the group's last tokens (N/2 per CTA, loaded with the 64-row
-// box), so the tile's MMA work follows its tokens. An M = 128 two-SM MMA keeps the tensor
-// pipes as busy as an M = 256 one (measured: every k-block of a 128-row tail took as long
-// as a full tile's on the DeepSeek-V2-shaped layer, where 87 of 338 row tiles are tails).
+// N = 32 .. 192 columns are the group's last tokens (N/2 per CTA, loaded with the 64-row
+// box up to N = 128, the 128-row box above), so the tile's MMA work follows its tokens.
+// It takes as long as a full tile (a fixed cost per MMA instruction) but does less tensor
+// work, which under the power cap is clock: on the DeepSeek-V2-shaped layer (87 tails
+// <= 128 rows and 71 remainders of 129-255 rows in 338 row tiles) swapping remainders up
+// to 192 rows took the FFN 2.36 -> 2.31 ms. Past 192 rows the savings are small and the
+// token-by-token epilogue of a wide swapped tile costs more than it saves (swapping every
+// partial tile made the Qwen3- and Mixtral-shaped FFNs, whose remainders are 224-255
+// rows, 40 % and 7 % slower).
 // The accumulator of a swapped tile is transposed: TMEM lane = weight row (up: lanes 0-63
 // the gate and 64-127 the up value of the CTA's 64 features; down: the CTA's 128 output
 // columns), TMEM column = token; its epilogue writes the output token by token.
@@ -498,7 +503,7 @@ __device__ __forceinline__ void decode_pair_tile(const int32_t* ts, const int32_
   r.g = g;
   r.rows = shared ? p.T : eo[g + 1] - eo[g];
   const int rem = r.rows - m_pair * 256;
-  r.swap = rem <= 128;
+  r.swap = rem <= 192;  // (see the two-SM variant's notes above)
   r.N = r.swap ? (rem + 31) & ~31 : 256;
   // this CTA's first operand row: its 128 of a 256-row tile, or its N/2 of the tokens
   r.m0 = m_pair * 256 + (int)rank * (r.swap ? r.N / 2 : 128);
@@ -592,11 +597,12 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,     // 128-row
       Tile tl;
       decode_pair_tile<UP>(s_ts, s_eo, p, t, rank, tl);
       // token rows: 128 (256-row tile) or a 64-row box holding the CTA's N/2 <= 64 tokens
-      const CUtensorMap* amap = tl.swap ? (tl.a_shared ? &tmA_sh64 : &tmA64)
-                                        : (tl.a_shared ? &tmA_sh : &tmA);
-      const uint32_t tx = 2 * ((tl.swap ? kPairStage / 2 : kPairStage) + kPairStage);
+      const bool box64 = tl.swap && tl.N <= 128;  // the CTA's N/2 tokens fit a 64-row box
+      const CUtensorMap* amap = box64 ? (tl.a_shared ? &tmA_sh64 : &tmA64)
+                                      : (tl.a_shared ? &tmA_sh : &tmA);
+      const uint32_t tx = 2 * ((box64 ? kPairStage / 2 : kPairStage) + kPairStage);
       if (UP && p.g_src && !tl.a_shared &&
-          !wait_rows(p, tl.a_row, min(tl.a_row + (tl.swap ? 64 : 128), s_eo[tl.g + 1]), abort)) {
+          !wait_rows(p, tl.a_row, min(tl.a_row + (box64 ? 64 : 128), s_eo[tl.g + 1]), abort)) {
         ok = false;
         break;
       }

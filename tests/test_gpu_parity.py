@@ -681,12 +681,13 @@ def test_expert_ffn_two_sm_tiles_ragged(T, E, K, S, d, F):
 @pytest.mark.parametrize("d,F", [(384, 704), (256, 256)])
 def test_expert_ffn_two_sm_tail_tiles(d, F):
     """Two-SM tiles end a group with a swapped tile (weight rows as the MMA's 256 rows, the
-    group's last tokens as its N = 32 .. 128 columns) when its last rows fit in 128 and
+    group's last tokens as its N = 32 .. 192 columns) when its last rows fit in 192 and
     with a full 256-row tile otherwise. Expert segments of 64, 300, 450, 0, 129, 128, 513
     and 257 rows hit every case (a group that is only a swapped tile, swapped tails of 44,
-    1 and 1 rows, a 128-row swapped group, a 194-row M = 256 tail, a 129-row group, an
-    empty group), and the shared expert's 1100 rows end in a 76-row swapped tail; F = 704
-    and d = 384 leave half-valid last n-tiles in the up and the down GEMM."""
+    1 and 1 rows, a 128-row swapped group, a 129-row group whose N = 160 tokens come
+    through the 128-row box, a 194-row M = 256 tail, an empty group), and the shared
+    expert's 1100 rows end in a 76-row swapped tail; F = 704 and d = 384 leave half-valid
+    last n-tiles in the up and the down GEMM."""
     counts = [64, 300, 450, 0, 129, 128, 513, 257]
     E, K, S, T = len(counts), 2, 1, 1100
     assert T * K >= 256 * E and sum(counts) <= T * K
@@ -724,8 +725,9 @@ def test_expert_ffn_two_sm_tail_tiles(d, F):
 def test_expert_ffn_two_sm_tail_mixes(counts, S, T):
     """Two-SM tiles on row mixes at the extremes: every group ending in a 44-row swapped
     tail, no tail at all (whole 256-row tiles only), and ragged groups (1, 3 and 44 rows,
-    255 and 129, empty, multiples of 256) with a shared expert. Every row equals the
-    oracle's expert FFN; rows past the last group are not written."""
+    129 and 188-row swapped remainders, 255-, 232- and 208-row M = 256 ones, empty groups,
+    multiples of 256) with a shared expert. Every row equals the oracle's expert FFN; rows
+    past the last group are not written."""
     d, F, K = 256, 256, 2
     E = len(counts)
     assert T * K >= 256 * E and sum(counts) <= T * K
