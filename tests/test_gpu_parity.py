@@ -760,6 +760,49 @@ def test_expert_ffn_two_sm_tail_mixes(counts, S, T):
         assert rel_err_rows(to_np(ysh[j]), O.swiglu_ffn(xn, *W[E + j])).max() <= VALUE_TOL
 
 
+@pytest.mark.parametrize("seed", range(6))
+def test_expert_ffn_random_row_mixes(seed):
+    """Two-SM expert FFN on seeded random row counts (a skewed draw with empty and 1-row
+    groups, remainders on both sides of 128 and 192, a shared expert on odd seeds),
+    against the oracle's expert FFN row by row."""
+    rng = np.random.default_rng(1000 + seed)
+    E, K, d, F = 16, 2, 256, 320
+    counts = rng.choice([0, 1, 37, 129, 160, 192, 193, 255, 256, 300, 449, 520, 700],
+                        size=E).astype(np.int64)
+    S = seed % 2
+    T = max(int(counts.sum()) // K + 1, 256 * E // K)   # two-SM tiles: T K >= 256 E
+    assert T * K >= 256 * E and counts.sum() <= T * K
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    x = torch.randn(T, d, generator=g, device="cuda").to(torch.bfloat16)
+    xd = torch.randn(T * K, d, generator=g, device="cuda").to(torch.bfloat16)
+    w1 = (torch.randn(E + S, F, d, generator=g, device="cuda") / d ** 0.5).to(torch.bfloat16)
+    w3 = (torch.randn(E + S, F, d, generator=g, device="cuda") / d ** 0.5).to(torch.bfloat16)
+    w2 = (torch.randn(E + S, d, F, generator=g, device="cuda") / F ** 0.5).to(torch.bfloat16)
+    eo_n = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    desc = smoe.make_desc(T, d, E, K, 1, F, S, 2, 100, "bf16")
+    ws = smoe.workspace(desc)
+    yd = torch.full_like(xd, 7.0)
+    ysh = torch.empty(S, T, d, dtype=torch.bfloat16, device="cuda") if S else None
+    smoe.smoe_expert_ffn(desc, xd, torch.as_tensor(eo_n, device="cuda"), w1, w3, w2, yd, ws,
+                         x=x, y_shared=ysh)
+    smoe.smoe_get_status(ws)
+    torch.cuda.synchronize()
+    xdn, xn = to_np(xd).astype(np.float64), to_np(x).astype(np.float64)
+    W = [tuple(to_np(m[e]).astype(np.float64) for m in (w1, w3, w2)) for e in range(E + S)]
+    y = to_np(yd)
+    n = eo_n[-1]
+    ref = np.zeros((n, d))
+    for e in range(E):
+        lo, hi = eo_n[e], eo_n[e + 1]
+        if hi > lo:
+            ref[lo:hi] = O.swiglu_ffn(xdn[lo:hi], *W[e])
+    if n:
+        assert rel_err_rows(y[:n], ref).max() <= VALUE_TOL
+    assert (y[n:] == 7.0).all()
+    for j in range(S):
+        assert rel_err_rows(to_np(ysh[j]), O.swiglu_ffn(xn, *W[E + j])).max() <= VALUE_TOL
+
+
 @pytest.mark.parametrize("name,T", [("tiny_fp32", None), ("dsv2_prefill", 1537), ("qwen3_foe", 3001),
                                     ("dsv2_prefill", None)],
                          ids=["tiny", "dsv2-T1537", "qwen3-T3001", "dsv2-full"])
