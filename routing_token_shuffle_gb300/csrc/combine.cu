@@ -121,8 +121,9 @@ combine_kernel(const uint4* __restrict__ y_disp, const int32_t* __restrict__ pai
   }
 }
 
-// The combine follows the expert FFN's persistent down GEMM: launched in plain stream
-// order (see launch_k_serial).
+// The combine follows the expert FFN's persistent down GEMM with programmatic launch; the
+// down GEMM lets it be scheduled only as the GEMM's CTAs finish (pdl_trigger at its end),
+// so its CTAs never sit resident beside the GEMM's.
 template <typename TE>
 cudaError_t launch_combine_t(const smoe_desc& d, const void* y_disp, const int32_t* pair_row,
                              const float* w, const void* y_sh, void* y, int S, int nvec,
@@ -133,19 +134,19 @@ cudaError_t launch_combine_t(const smoe_desc& d, const void* y_disp, const int32
   const int rows = d.T * d.K;
   if (S > 0) {  // K + S > 2 always holds here (K >= 1)
     if (d.K + S <= 4)
-      SMOE_LAUNCH_SERIAL((combine_kernel<TE, 2, true>), d.T, kThreads, 0, s, yd, pair_row, w, ys, yo, d.T,
+      SMOE_LAUNCH((combine_kernel<TE, 2, true>), d.T, kThreads, 0, s, yd, pair_row, w, ys, yo, d.T,
                   d.K, S, nvec, rows, st);
     else
-      SMOE_LAUNCH_SERIAL((combine_kernel<TE, 1, true>), d.T, kThreads, 0, s, yd, pair_row, w, ys, yo, d.T,
+      SMOE_LAUNCH((combine_kernel<TE, 1, true>), d.T, kThreads, 0, s, yd, pair_row, w, ys, yo, d.T,
                   d.K, S, nvec, rows, st);
   } else if (d.K <= 2) {
-    SMOE_LAUNCH_SERIAL((combine_kernel<TE, 4, false>), d.T, kThreads, 0, s, yd, pair_row, w, ys, yo, d.T,
+    SMOE_LAUNCH((combine_kernel<TE, 4, false>), d.T, kThreads, 0, s, yd, pair_row, w, ys, yo, d.T,
                 d.K, S, nvec, rows, st);
   } else if (d.K <= 4) {
-    SMOE_LAUNCH_SERIAL((combine_kernel<TE, 2, false>), d.T, kThreads, 0, s, yd, pair_row, w, ys, yo, d.T,
+    SMOE_LAUNCH((combine_kernel<TE, 2, false>), d.T, kThreads, 0, s, yd, pair_row, w, ys, yo, d.T,
                 d.K, S, nvec, rows, st);
   } else {
-    SMOE_LAUNCH_SERIAL((combine_kernel<TE, 1, false>), d.T, kThreads, 0, s, yd, pair_row, w, ys, yo, d.T,
+    SMOE_LAUNCH((combine_kernel<TE, 1, false>), d.T, kThreads, 0, s, yd, pair_row, w, ys, yo, d.T,
                 d.K, S, nvec, rows, st);
   }
   return cudaGetLastError();

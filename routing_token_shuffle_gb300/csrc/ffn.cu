@@ -199,7 +199,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmA_sh,
                     const __grid_constant__ CUtensorMap tmB1,
                     const __grid_constant__ CUtensorMap tmB3, const GemmArgs p) {
-  pdl_wait_and_trigger();
+  // the down GEMM lets the combine be scheduled only as its CTAs finish (see the end)
+  if (UP) pdl_wait_and_trigger(); else pdl_wait();
   using TE = typename std::conditional<F32, float, __nv_bfloat16>::type;
   constexpr int BK = F32 ? 32 : 64;           // elements per 128-byte row
   constexpr int kMmaK = F32 ? 8 : 16;          // elements per MMA
@@ -380,6 +381,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  if (!UP && threadIdx.x == 0) pdl_trigger();
   if (warp == 2) tc::tmem_dealloc(tmem, 2 * kAccCols);
 }
 
@@ -532,7 +534,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,     // 128-row
                          const __grid_constant__ CUtensorMap tmA_sh64,
                          const __grid_constant__ CUtensorMap tmB1,
                          const __grid_constant__ CUtensorMap tmB3, const GemmArgs p) {
-  pdl_wait_and_trigger();
+  // the down GEMM lets the combine be scheduled only as its CTAs finish (see the end)
+  if (UP) pdl_wait_and_trigger(); else pdl_wait();
   using TE = __nv_bfloat16;
   constexpr uint32_t kIdesc = tc::instr_desc(false, 256, 256);
 
@@ -804,6 +807,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,     // 128-row
   __syncthreads();
   tc::cluster_sync();
   tc::fence_after_sync();
+  if (!UP && threadIdx.x == 0) pdl_trigger();
   if (warp == 2) tc::tmem_dealloc_pair(tmem, 2 * kAccCols);
 }
 

@@ -120,14 +120,22 @@ extern thread_local unsigned long long g_kernel_launches;
 #define SMOE_COUNT_LAUNCH(n) (::smoe::g_kernel_launches += (n))
 
 // ---------------------------------------------------------------- dependent launch
-// Every library kernel but the combine (launch_k_serial) is launched with programmatic
-// stream serialisation and starts with
+// Every library kernel is launched with programmatic stream serialisation and starts with
 // pdl_wait() (griddepcontrol.wait: the previous kernel in the stream has completed and its
 // writes are visible) before touching global memory, then pdl_trigger() so that the next
-// kernel's CTAs may be scheduled while this grid drains. Without a programmatic
+// kernel's CTAs may be scheduled while this grid drains; the expert FFN's down GEMM
+// triggers only at its end instead, because its CTAs hold every SM and a combine made
+// resident beside them slowed the Qwen3-shaped step by ~24 us. Without a programmatic
 // predecessor the wait returns at once.
 __device__ __forceinline__ void pdl_wait_and_trigger() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// The two halves, for a kernel that lets its dependents be scheduled only at its end
+// (the expert FFN's down GEMM, whose CTAs hold every SM: the combine that follows is
+// then launched as the GEMM's CTAs finish, instead of resident beside them).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
@@ -148,25 +156,6 @@ inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_
   return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
 }
 
-// A kernel that follows a long persistent GEMM: launched programmatically, its CTAs
-// become resident beside the GEMM's (whose CTAs all start at once) and wait there for
-// the whole GEMM, which slowed the Qwen3-shaped step by ~24 us. Plain stream order.
-template <typename... KArgs, typename... Args>
-inline cudaError_t launch_k_serial(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                                   cudaStream_t s, Args&&... args) {
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 0;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  SMOE_COUNT_LAUNCH(1);
-  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
-}
 
 #define SMOE_LAUNCH(kern, grid, block, smem, stream, ...)                              \
   do {                                                                                 \
@@ -175,12 +164,6 @@ inline cudaError_t launch_k_serial(void (*kern)(KArgs...), dim3 grid, dim3 block
     if (le_ != cudaSuccess) return le_;                                                \
   } while (0)
 
-#define SMOE_LAUNCH_SERIAL(kern, grid, block, smem, stream, ...)                       \
-  do {                                                                                 \
-    cudaError_t le_ = ::smoe::launch_k_serial(kern, dim3(grid), dim3(block), smem,      \
-                                              stream, __VA_ARGS__);                    \
-    if (le_ != cudaSuccess) return le_;                                                \
-  } while (0)
 
 // The same for functions that return an smoe_status.
 #define SMOE_LAUNCH_STATUS(kern, grid, block, smem, stream, ...)                       \
